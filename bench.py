@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Benchmark: W1.58A8 ternary GEMV effective HBM GB/s and us per 2B-shaped decode layer.
+
+One step = one pass of the decode hot path over a 2B-shaped decoder stack at batch 1:
+30 distinct layers (521 MB of packed weights, > 4x the 126 MB L2, so the timed
+region streams HBM without any flush), each layer running
+
+    [RMSNorm+quant](x_attn) -> GEMV q|k|v (3840x2560) -> [quant](x_o) -> GEMV o (2560x2560)
+    -> [RMSNorm+quant](x_ffn) -> GEMV gate|up (13824x2560) -> [quant](x_down) -> GEMV down (2560x6912)
+
+with each bracketed quantisation fused into its GEMV launch (tw_quant_gemv, chained by
+programmatic dependent launch); --separate runs them as their own kernels.  Attention
+and the FFN activation are not part of the path: the o and down inputs are fresh
+N(0,1) vectors per layer.  Weights are N(0,1) drawn on the GPU (seeded torch generator)
+and absmean-ternarised once with tw_pack_ternary before timing (the conversion is
+offline).  The launches of a step are captured in one CUDA graph.
+
+value   = algorithmic bytes of all GEMVs in the step (packed weights + int8 activations
+          + scales) / device time of the step, whole job (all ranks).
+e2e     = the same metric with the step's inputs copied from pinned host memory and all
+          outputs copied back inside the timed region (one copy each way).
+roofline: the GEMV kernel; per-launch durations from CUDA events around each GEMV launch
+          of extra steps enqueued behind a short GPU sleep (so host launch overhead does
+          not show), bytes per launch from the shapes; peak = measured HBM copy rate.
+cpu_baseline / --impl reference: the CPU oracle (oracle/), as it stands, on the host.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling,
+no data-path collective); rank 0 prints max-over-ranks time and the summed bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W1.58A8 GEMV effective HBM GB/s (% of B300 peak); us per 2B-shaped decode layer"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6400.0
+LAYERS = 30
+MODEL = "2B"
+WORKLOAD = "2B-shaped decoder layer, batch 1 (hidden 2560, ffn 6912, 20/5 heads), 30 distinct layers"
+GEMV_SOURCES = ["ternary_weight_quant_b300/csrc/tw_gemv_stream.cu", "ternary_weight_quant_b300/csrc/tw_common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_dram_traffic.json")
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def combine_over_ranks(elapsed_s: float, units: float, world: int):
+    """Max elapsed time and summed units over ranks (identity when world == 1)."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ shapes and bytes
+def layer_plan():
+    import seeded_inputs as si
+    s = si.fused_layer_shapes(MODEL)
+    # (name, N, K, prologue) in step order; prologue: "rms" = RMSNorm+quant, "quant" = quant only
+    return [("qkv", *s["qkv"], "rms"), ("o", *s["o"], "quant"), ("gateup", *s["gateup"], "rms"),
+            ("down", *s["down"], "quant")]
+
+
+def gemv_bytes(N, K, M=1):
+    """Algorithmic bytes of one GEMV launch: packed weights + int8 activations + scales."""
+    return N * K // 4 + M * K + 4 + 4 * M
+
+
+def step_bytes(M=1):
+    return LAYERS * sum(gemv_bytes(N, K, M) for _, N, K, _ in layer_plan())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per GEMV launch from the committed ncu summary, if the kernel is unchanged."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    if d.get("source_hash") != source_hash(GEMV_SOURCES):
+        return None
+    return d.get("bytes_per_step_launch_avg")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.index, self.period = index, period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        import subprocess
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)  # let the first samples arrive before the timed work starts
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for line in self.lines:
+            f = [v.strip() for v in line.split(",")]
+            if len(f) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, f[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+def oracle_layer_sample(layer_data, seconds_min: float, seconds_max: float):
+    """Run the oracle's decode-layer sequence over host copies of layers until >= seconds_min.
+
+    Returns (bytes processed, elapsed seconds, layers run)."""
+    import oracle
+    import seeded_inputs as si
+    t0 = time.perf_counter()
+    done_bytes, n = 0, 0
+    plan = layer_plan()
+    while True:
+        L = layer_data[n % len(layer_data)]
+        for name, N, K, pro in plan:
+            x = L["x"][name]
+            if pro == "rms":
+                xq, sx, _ = oracle.rmsnorm_quant_act(x, L["g"][name], si.RMS_EPS)
+            else:
+                xq, sx, _ = oracle.quant_act(x)
+            oracle.ternary_matmul(L["packed"][name], L["gamma"][name], xq, sx)
+            done_bytes += gemv_bytes(N, K)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_min or el >= seconds_max:
+            return done_bytes, el, n
+
+
+def host_oracle_layers(n_layers: int, seed: int = 4242):
+    """Seeded host inputs for the oracle sample: same shapes and recipe as the GPU workload."""
+    import oracle
+    import seeded_inputs as si
+    out = []
+    for l in range(n_layers):
+        g = si.cpu_generator(seed + l)
+        L = {"packed": {}, "gamma": {}, "x": {}, "g": {}}
+        for name, N, K, pro in layer_plan():
+            W = si.weights(N, K, gen=g)
+            L["packed"][name], L["gamma"][name] = oracle.pack_ternary(W)
+            L["x"][name] = si.activations(1, K, gen=g)
+            if pro == "rms":
+                L["g"][name] = si.rms_gain(K, seed=seed + l)
+        out.append(L)
+    return out
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    layers = host_oracle_layers(1)
+    for _ in range(args.warmup):
+        oracle_layer_sample(layers, 0.0, 0.0)
+    t0 = time.perf_counter()
+    total_bytes = 0
+    for _ in range(args.steps):
+        b, _, _ = oracle_layer_sample(layers, 0.0, 0.0)  # one layer per step
+        total_bytes += b
+    el = time.perf_counter() - t0
+    value = total_bytes / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD + "; oracle step = one layer (bounded sample)", "M": 1},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "one 2B-shaped layer per step (RMSNorm/quant + 4 GEMVs), single thread"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU workload
+class DecodeStack:
+    """30 layers of packed weights, activations and outputs resident on the GPU.
+
+    All activation inputs of a step live in one flat device buffer and all outputs in
+    another, so the end-to-end measurement moves each direction in one copy."""
+
+    def __init__(self, tw, layers: int, M: int = 1, seed: int = 1234):
+        import torch
+        import seeded_inputs as si
+        self.tw, self.M, self.layers = tw, M, layers
+        self.plan = layer_plan()
+        n_in = layers * sum(M * K for _, N, K, _ in self.plan)
+        n_out = layers * sum(M * N for _, N, K, _ in self.plan)
+        self.x_all = torch.empty(n_in, dtype=torch.float32, device="cuda")
+        self.y_all = torch.empty(n_out, dtype=torch.float32, device="cuda")
+        self.L = []
+        ws = torch.empty(tw.tw_pack_workspace_bytes(13824, 2560), dtype=torch.uint8, device="cuda")
+        oi = oo = 0
+        for l in range(layers):
+            d = {}
+            for i, (name, N, K, pro) in enumerate(self.plan):
+                W = si.device_normal((N, K), seed=seed + 1000 * l + i)
+                packed = torch.empty((N, K // 4), dtype=torch.uint8, device="cuda")
+                gamma = torch.empty(1, dtype=torch.float32, device="cuda")
+                tw.tw_pack_ternary(W, packed, gamma, ws)
+                del W
+                x = self.x_all[oi:oi + M * K].view(M, K)
+                oi += M * K
+                x.copy_(si.device_normal((M, K), seed=seed + 1000 * l + 100 + i))
+                y = self.y_all[oo:oo + M * N].view(M, N)
+                oo += M * N
+                g = (1.0 + 0.1 * si.device_normal((K,), seed=seed + 1000 * l + 200 + i)) if pro == "rms" else None
+                d[name] = dict(packed=packed, gamma=gamma, x=x, g=g, N=N, K=K, pro=pro, y=y,
+                               x_q=torch.empty((M, K), dtype=torch.int8, device="cuda"),
+                               s_x=torch.empty(M, dtype=torch.float32, device="cuda"),
+                               x_sum=torch.empty(M, dtype=torch.int32, device="cuda"))
+            self.L.append(d)
+        torch.cuda.synchronize()
+
+    def launches_per_step(self, fused=True):
+        return self.layers * len(self.plan) * (1 if fused else 2)
+
+    def enqueue(self, events=None, fused=True):
+        """Enqueue one step on the current stream (optionally with events around each GEMV).
+
+        fused: one tw_quant_gemv launch per GEMV (quantisation fused in, programmatic
+        dependent launch); otherwise tw_rmsnorm_quant_act / tw_quant_act + tw_ternary_gemv."""
+        import seeded_inputs as si
+        tw = self.tw
+        for d in self.L:
+            for name, N, K, pro in self.plan:
+                e = d[name]
+                if not fused:
+                    if pro == "rms":
+                        tw.tw_rmsnorm_quant_act(e["x"], e["g"], si.RMS_EPS, e["x_q"], e["s_x"], e["x_sum"])
+                    else:
+                        tw.tw_quant_act(e["x"], e["x_q"], e["s_x"], e["x_sum"])
+                if events is not None:
+                    a, b = events_new(), events_new()
+                    a.record()
+                if fused:
+                    tw.tw_quant_gemv(e["x"], e["packed"], e["gamma"], e["y"], g=e["g"], eps=si.RMS_EPS)
+                else:
+                    tw.tw_ternary_gemv(e["packed"], e["gamma"], e["x_q"], e["s_x"], e["y"], e["x_sum"])
+                if events is not None:
+                    b.record()
+                    events.append((name, a, b))
+
+
+def events_new():
+    import torch
+    return torch.cuda.Event(enable_timing=True)
+
+
+def gpu_sleep(ms: float):
+    """Keep the current stream busy for about `ms` (torch's bounded spin kernel; ~2 GHz clock)."""
+    import torch
+    torch.cuda._sleep(int(ms * 2.0e6))
+
+
+def capture(stack, fused):
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        stack.enqueue(fused=fused)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        stack.enqueue(fused=fused)
+    return graph
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    import ternary_weight_quant_b300 as tw
+
+    fused = not args.separate
+    stack = DecodeStack(tw, LAYERS, M=1)
+    bytes_per_step = step_bytes(1)
+    graph = capture(stack, fused)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays
+    start, stop = events_new(), events_new()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall0 = time.perf_counter()
+        start.record()
+        for _ in range(args.steps):
+            graph.replay()
+        stop.record()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    elapsed = start.elapsed_time(stop) / 1e3
+    elapsed_max, total_bytes = combine_over_ranks(elapsed, bytes_per_step * args.steps, world)
+    value = total_bytes / elapsed_max / 1e9
+    ms_per_step = elapsed_max / args.steps * 1e3
+    us_per_layer = ms_per_step * 1e3 / LAYERS
+
+    # ---- roofline of the GEMV kernel: events around each GEMV launch of extra steps
+    per_launch = {}
+    for rep in range(3):
+        evs = []
+        gpu_sleep(30.0)
+        stack.enqueue(events=evs, fused=fused)
+        torch.cuda.synchronize()
+        if rep == 0:
+            continue
+        for name, a, b in evs:
+            per_launch.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
+    gemv_time = sum(sum(v) for v in per_launch.values())
+    gemv_launches = sum(len(v) for v in per_launch.values())
+    shapes = {name: (N, K) for name, N, K, _ in layer_plan()}
+    gemv_bytes_total = sum(gemv_bytes(*shapes[n]) * len(v) for n, v in per_launch.items())
+    achieved = gemv_bytes_total / gemv_time / 1e9
+    peak, peak_kind = measured_peaks()
+    per_shape = {n: {"bytes": gemv_bytes(*shapes[n]), "us_median": statistics.median(v) * 1e6,
+                     "GB/s": gemv_bytes(*shapes[n]) / statistics.median(v) / 1e9}
+                 for n, v in per_launch.items()}
+
+    # ---- e2e: inputs from pinned host, outputs back to pinned host, per step (one copy each way)
+    h_in = stack.x_all.cpu().pin_memory()
+    h_out = torch.empty(stack.y_all.shape, dtype=torch.float32).pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        stack.x_all.copy_(h_in, non_blocking=True)
+        graph.replay()
+        h_out.copy_(stack.y_all, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 500))
+    barrier(world)
+    e0, e1 = events_new(), events_new()
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_el, e2e_bytes = combine_over_ranks(e0.elapsed_time(e1) / 1e3, bytes_per_step * e2e_steps, world)
+    e2e_value = e2e_bytes / e2e_el / 1e9
+
+    # ---- CPU baseline: the oracle on the host, bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        layers = host_oracle_layers(1)
+        b, el, n = oracle_layer_sample(layers, args.cpu_seconds, 3 * args.cpu_seconds)
+        cpu = {"value": b / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} run(s) of one 2B-shaped layer (RMSNorm/quant + 4 GEMVs, M=1), "
+                         f"single thread, {el:.1f} s"}
+
+    if rank == 0:
+        kern = "tw::gemv_stream_kernel<1,8,fused>" if fused else "tw::gemv_stream_kernel<1,8>"
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": 1, "layers": LAYERS, "hidden": 2560, "ffn": 6912,
+                       "bytes_per_step": bytes_per_step, "launches_per_step": stack.launches_per_step(fused),
+                       "quantisation": "fused into the GEMV launch" if fused else "separate kernels",
+                       "graph": "one CUDA graph per step",
+                       "l2": "working set 521 MB > 4x the 126 MB L2; no flush needed",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_layer": us_per_layer,
+            "pct_of_nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
+            "pct_of_measured_copy": 100.0 * value / world / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": recorded_traffic(),
+                         "kernel": kern, "peak_source": peak_kind,
+                         "launches_timed": gemv_launches, "per_shape": per_shape},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": stack.launches_per_step(fused) * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--separate", action="store_true", help="quantisation as separate kernels")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

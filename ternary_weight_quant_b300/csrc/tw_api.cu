@@ -1,0 +1,269 @@
+// tw_api.cu -- the C ABI of libtw.so: argument checks, then kernel launches.
+//
+// This is the boundary between a host runtime and the kernels, the role the
+// "1bit-systems" page gives its FFI layer (系统组件全景).  Every entry point
+// checks its arguments on the host in a fixed order -- NULL pointers, shapes,
+// alignment, then (with one CUDA query per pointer) that each pointer is device
+// memory -- and enqueues nothing when a check fails.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "../../include/ternary_w158a8.h"
+
+cudaError_t tw_launch_pack(const float* W, long long N, long long K, uint8_t* packed, float* w_scale,
+                           void* workspace, cudaStream_t stream, int num_sms);
+size_t tw_pack_ws_size();
+cudaError_t tw_launch_quant_act(const float* x, long long M, long long K, int8_t* x_q, float* s_x,
+                                int32_t* x_sum, cudaStream_t stream);
+cudaError_t tw_launch_rmsnorm_quant_act(const float* x, const float* g, float eps, long long M, long long K,
+                                        int8_t* x_q, float* s_x, int32_t* x_sum, cudaStream_t stream);
+cudaError_t tw_launch_gemv(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
+                           const int32_t* x_sum, int M, int N, int K, float* y, int32_t* acc_out,
+                           cudaStream_t stream);
+cudaError_t tw_launch_gemv_generic(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
+                                   const float* s_x, int M, int N, int K, float* y, int32_t* acc_out,
+                                   cudaStream_t stream);
+int tw_stream_supported(int M, int N, int K, int num_sms);
+cudaError_t tw_launch_gemv_stream(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
+                                  const float* s_x, int M, int N, int K, float* y, int32_t* acc_out,
+                                  cudaStream_t stream, int num_sms, bool pdl);
+cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, const uint8_t* packed,
+                                 const float* w_scale, int M, int N, int K, float* y, int8_t* x_q_out,
+                                 float* s_x_out, int32_t* x_sum_out, int32_t* acc_out, cudaStream_t stream,
+                                 int num_sms, bool pdl);
+cudaError_t tw_read_stream_status(int* out);
+cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
+                           int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream, int num_sms,
+                           int* unsupported);
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];  // 0 = unknown, -1 = not sm_103, else SM count
+
+// Current device must be an sm_103 part; returns its SM count or a status.
+tw_status device_info(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return TW_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return TW_ERR_UNSUPPORTED;
+  int v = g_sms[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return TW_ERR_CUDA;
+    }
+    v = (major == 10 && minor == 3) ? n : -1;
+    g_sms[dev].store(v, std::memory_order_relaxed);
+  }
+  if (v < 0) return TW_ERR_UNSUPPORTED;
+  *sms = v;
+  return TW_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device or managed memory only (pageable or pinned host memory is rejected).
+tw_status check_device_ptr(const void* p) {
+  if (!p) return TW_OK;
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return TW_ERR_NOT_DEVICE_PTR;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return TW_ERR_NOT_DEVICE_PTR;
+  return TW_OK;
+}
+
+template <typename... P>
+tw_status check_device_ptrs(const P*... ps) {
+  tw_status st = TW_OK;
+  ((st = (st == TW_OK ? check_device_ptr(ps) : st)), ...);
+  return st;
+}
+
+tw_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TW_OK : TW_ERR_CUDA; }
+
+tw_status check_kdim(int64_t K) {
+  if (K < 4 || K > TW_MAX_K || K % 4 != 0) return TW_ERR_SHAPE;
+  return TW_OK;
+}
+
+tw_status check_product_args(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
+                             const float* s_x, int64_t M, int64_t N, int64_t K, float* y) {
+  if (!packed || !w_scale || !x_q || !s_x || !y) return TW_ERR_NULL;
+  if (M < 1 || N < 1 || check_kdim(K) != TW_OK) return TW_ERR_SHAPE;
+  if (N > (1LL << 31) - 1 || M > (1LL << 31) - 1 || N * K >= TW_MAX_NK) return TW_ERR_SHAPE;
+  if (M * N >= (1LL << 40) || M * K >= (1LL << 40)) return TW_ERR_SHAPE;
+  if (!aligned(w_scale, 4) || !aligned(s_x, 4) || !aligned(y, 4)) return TW_ERR_ALIGN;
+  return TW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+TW_API const char* tw_status_string(int status) {
+  switch (status) {
+    case TW_OK: return "TW_OK";
+    case TW_ERR_NULL: return "TW_ERR_NULL: a required pointer is NULL";
+    case TW_ERR_SHAPE: return "TW_ERR_SHAPE: M, N or K out of range, K % 4 != 0, or size overflow";
+    case TW_ERR_ALIGN: return "TW_ERR_ALIGN: a pointer lacks its required alignment";
+    case TW_ERR_NOT_DEVICE_PTR: return "TW_ERR_NOT_DEVICE_PTR: a pointer is not device memory";
+    case TW_ERR_CUDA: return "TW_ERR_CUDA: the CUDA runtime reported an error";
+    case TW_ERR_UNSUPPORTED: return "TW_ERR_UNSUPPORTED: no sm_103 device or unsupported case";
+    case TW_ERR_TIMEOUT: return "TW_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case TW_ERR_WORKSPACE: return "TW_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown tw_status";
+  }
+}
+
+TW_API int tw_version(void) { return 100; }
+
+TW_API size_t tw_pack_workspace_bytes(int64_t N, int64_t K) {
+  if (N < 1 || check_kdim(K) != TW_OK || N * K >= TW_MAX_NK) return 0;
+  return tw_pack_ws_size();
+}
+
+TW_API tw_status tw_pack_ternary(const float* W, int64_t N, int64_t K, uint8_t* packed, float* w_scale,
+                                 void* workspace, size_t ws_bytes, tw_stream_t stream) {
+  if (!W || !packed || !w_scale) return TW_ERR_NULL;
+  if (N < 1 || check_kdim(K) != TW_OK || N * K >= TW_MAX_NK) return TW_ERR_SHAPE;
+  if (!workspace || ws_bytes < tw_pack_ws_size()) return TW_ERR_WORKSPACE;
+  if (!aligned(W, 16) || !aligned(packed, 4) || !aligned(w_scale, 4) || !aligned(workspace, 8))
+    return TW_ERR_ALIGN;
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(W, packed, w_scale, static_cast<const uint8_t*>(workspace));
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_pack(W, N, K, packed, w_scale, workspace, (cudaStream_t)stream, sms));
+}
+
+TW_API tw_status tw_quant_act(const float* x, int64_t M, int64_t K, int8_t* x_q, float* s_x, int32_t* x_sum,
+                              tw_stream_t stream) {
+  if (!x || !x_q || !s_x) return TW_ERR_NULL;
+  if (M < 1 || M > (1LL << 20) || check_kdim(K) != TW_OK) return TW_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(x_q, 4) || !aligned(s_x, 4) || !aligned(x_sum, 4)) return TW_ERR_ALIGN;
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(x, x_q, s_x, x_sum);
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_quant_act(x, M, K, x_q, s_x, x_sum, (cudaStream_t)stream));
+}
+
+TW_API tw_status tw_rmsnorm_quant_act(const float* x, const float* g, float eps, int64_t M, int64_t K,
+                                      int8_t* x_q, float* s_x, int32_t* x_sum, tw_stream_t stream) {
+  if (!x || !g || !x_q || !s_x) return TW_ERR_NULL;
+  if (M < 1 || M > (1LL << 20) || check_kdim(K) != TW_OK) return TW_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(x_q, 4) || !aligned(s_x, 4) || !aligned(x_sum, 4))
+    return TW_ERR_ALIGN;
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(x, g, x_q, s_x, x_sum);
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_rmsnorm_quant_act(x, g, eps, M, K, x_q, s_x, x_sum, (cudaStream_t)stream));
+}
+
+TW_API tw_status tw_ternary_gemv(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
+                                 const float* s_x, const int32_t* x_sum, int64_t M, int64_t N, int64_t K,
+                                 float* y, int32_t* acc_out, tw_stream_t stream) {
+  tw_status st = check_product_args(packed, w_scale, x_q, s_x, M, N, K, y);
+  if (st != TW_OK) return st;
+  if (M > TW_GEMV_MAX_M) return TW_ERR_SHAPE;
+  if (!aligned(x_sum, 4) || !aligned(acc_out, 4)) return TW_ERR_ALIGN;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(packed, w_scale, x_q, s_x, x_sum, y, acc_out);
+  if (st != TW_OK) return st;
+  if (aligned(packed, 16) && aligned(x_q, 16) && tw_stream_supported((int)M, (int)N, (int)K, sms))
+    return from_cuda(tw_launch_gemv_stream(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
+                                           (cudaStream_t)stream, sms, false));
+  return from_cuda(tw_launch_gemv(packed, w_scale, x_q, s_x, x_sum, (int)M, (int)N, (int)K, y, acc_out,
+                                  (cudaStream_t)stream));
+}
+
+TW_API tw_status tw_quant_gemv(const float* x, const float* g, float eps, const uint8_t* packed,
+                               const float* w_scale, int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q_out,
+                               float* s_x_out, int32_t* x_sum_out, int32_t* acc_out, tw_stream_t stream) {
+  if (!x || !packed || !w_scale || !y) return TW_ERR_NULL;
+  if (M < 1 || M > TW_QUANT_GEMV_MAX_M || N < 1 || N > (1LL << 31) - 1 || check_kdim(K) != TW_OK ||
+      K % 64 != 0 || N * K >= TW_MAX_NK)
+    return TW_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(packed, 16) || !aligned(w_scale, 4) || !aligned(y, 4) ||
+      !aligned(x_q_out, 16) || !aligned(s_x_out, 4) || !aligned(x_sum_out, 4) || !aligned(acc_out, 4))
+    return TW_ERR_ALIGN;
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  if (!tw_stream_supported((int)M, (int)N, (int)K, sms)) return TW_ERR_UNSUPPORTED;
+  st = check_device_ptrs(x, g, packed, w_scale, y, x_q_out, s_x_out, x_sum_out, acc_out);
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_fused_gemv(x, g, eps, packed, w_scale, (int)M, (int)N, (int)K, y, x_q_out, s_x_out,
+                                        x_sum_out, acc_out, (cudaStream_t)stream, sms, true));
+}
+
+TW_API tw_status tw_ternary_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
+                                 const float* s_x, const int32_t* x_sum, int64_t M, int64_t N, int64_t K,
+                                 float* y, int32_t* acc_out, tw_stream_t stream) {
+  (void)x_sum;
+  tw_status st = check_product_args(packed, w_scale, x_q, s_x, M, N, K, y);
+  if (st != TW_OK) return st;
+  if (K % 16 != 0) return TW_ERR_SHAPE;
+  if (!aligned(x_q, 16) || !aligned(packed, 16) || !aligned(acc_out, 4)) return TW_ERR_ALIGN;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(packed, w_scale, x_q, s_x, y, acc_out);
+  if (st != TW_OK) return st;
+  int unsupported = 0;
+  cudaError_t e = tw_launch_gemm(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
+                                 (cudaStream_t)stream, sms, &unsupported);
+  if (unsupported) return TW_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+// Token count from which the tensor-core GEMM takes over (disabled until the GEMM is enabled).
+static const int64_t kGemmCrossoverM = INT64_MAX;
+
+TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
+                                   const float* s_x, const int32_t* x_sum, int64_t M, int64_t N, int64_t K,
+                                   float* y, int32_t* acc_out, tw_stream_t stream) {
+  tw_status st = check_product_args(packed, w_scale, x_q, s_x, M, N, K, y);
+  if (st != TW_OK) return st;
+  if (M <= TW_GEMV_MAX_M) return tw_ternary_gemv(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, stream);
+  if (M >= kGemmCrossoverM && K % 16 == 0 && aligned(x_q, 16) && aligned(packed, 16))
+    return tw_ternary_gemm(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, stream);
+  if (!aligned(acc_out, 4)) return TW_ERR_ALIGN;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(packed, w_scale, x_q, s_x, y, acc_out);
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_gemv_generic(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
+                                          (cudaStream_t)stream));
+}
+
+TW_API tw_status tw_device_status(int32_t* status) {
+  if (!status) return TW_ERR_NULL;
+  int v = 0;
+  if (tw_read_stream_status(&v) != cudaSuccess) {
+    cudaGetLastError();
+    return TW_ERR_CUDA;
+  }
+  *status = v;
+  return TW_OK;
+}
+
+}  // extern "C"

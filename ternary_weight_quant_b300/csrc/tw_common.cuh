@@ -1,0 +1,122 @@
+// tw_common.cuh -- small device helpers shared by the libtw kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ternary_w158a8.h"
+
+namespace tw {
+
+constexpr int kWarp = 32;
+
+// L2 policy for data read exactly once (the packed weights): evict first, so the
+// stream does not push the activations and outputs out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Streaming 32-bit load: read-only path, no L1 allocation, L2 evict-first hint.
+__device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p, uint64_t pol) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+  return v;
+}
+
+// Bucket decomposition of a finite fp32 magnitude: |v| = m * 2^(b-1) * 2^-149 with
+// m < 2^24 an integer and b = max(biased exponent, 1) in [1, 255].
+__device__ __forceinline__ void f32_bucket(float v, uint32_t& m, int& b) {
+  uint32_t bits = __float_as_uint(v) & 0x7fffffffu;
+  uint32_t e8 = bits >> 23;
+  uint32_t frac = bits & 0x7fffffu;
+  m = e8 ? (frac | 0x800000u) : frac;
+  b = e8 ? (int)e8 : 1;
+}
+
+// Exact value of  sum_b hist[b] * 2^(step*(b-1))  (hist[0] must be 0), rounded
+// once to the nearest double with ties to even, times 2^lsb_exp.  Called by one
+// full warp; every lane returns the result.  The integer is held as 32 base-2^32
+// digits, one per lane (1024 bits: enough for step <= 2 and 64-bit buckets).
+__device__ __forceinline__ double warp_exact_hist_to_double(const unsigned long long* hist,
+                                                            int nbuckets, int step, int lsb_exp) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  unsigned long long dig = 0;
+  for (int b0 = 0; b0 < nbuckets; b0 += 32) {
+    const unsigned long long hv = (b0 + lane < nbuckets) ? hist[b0 + lane] : 0ull;
+    unsigned nz = __ballot_sync(full, hv != 0ull);
+    while (nz) {
+      const int src = __ffs(nz) - 1;
+      nz &= nz - 1;
+      const unsigned long long v = __shfl_sync(full, hv, src);
+      const int pos = step * (b0 + src - 1);
+      const int d = pos >> 5, o = pos & 31;
+      const unsigned long long lo = v << o;
+      const unsigned long long hi = o ? (v >> (64 - o)) : 0ull;
+      const int r = lane - d;
+      const unsigned piece = r == 0 ? (unsigned)lo : r == 1 ? (unsigned)(lo >> 32) : r == 2 ? (unsigned)hi : 0u;
+      dig += piece;
+    }
+  }
+  // Carry propagation (each pass moves carries up one digit; a ripple across all
+  // 32 digits needs at most 33 passes).
+  for (int it = 0; it < 40; ++it) {
+    if (!__any_sync(full, (dig >> 32) != 0ull)) break;
+    const unsigned long long c = dig >> 32;
+    dig &= 0xffffffffull;
+    const unsigned long long cin = __shfl_up_sync(full, c, 1);
+    if (lane > 0) dig += cin;
+  }
+  const unsigned nzmask = __ballot_sync(full, dig != 0ull);
+  if (nzmask == 0u) return 0.0;
+  const int top = 31 - __clz(nzmask);
+  unsigned d2 = __shfl_sync(full, (unsigned)dig, top);
+  unsigned d1 = __shfl_sync(full, (unsigned)dig, top >= 1 ? top - 1 : 0);
+  unsigned d0 = __shfl_sync(full, (unsigned)dig, top >= 2 ? top - 2 : 0);
+  if (top < 1) d1 = 0u;
+  if (top < 2) d0 = 0u;
+  const bool sticky_low = top >= 3 && (nzmask & ((1u << (top - 2)) - 1u)) != 0u;
+  const int lz = __clz(d2);
+  unsigned __int128 w = ((unsigned __int128)d2 << 64) | ((unsigned __int128)d1 << 32) | d0;
+  w <<= (lz + 32);  // most significant set bit now at bit 127
+  unsigned long long m = (unsigned long long)(w >> 75);  // 53 bits
+  const bool round_bit = ((unsigned)(w >> 74) & 1u) != 0u;
+  const bool sticky = sticky_low || (w & (((unsigned __int128)1 << 74) - 1)) != 0;
+  if (round_bit && (sticky || (m & 1ull))) m += 1ull;
+  const int msb = 32 * top + 31 - lz;
+  return ldexp((double)m, msb - 52 + lsb_exp);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ int warp_sum(int v) { return __reduce_add_sync(0xffffffffu, v); }
+
+// Transpose the 4x4 bytes of a 16-byte activation group so that word s holds
+// x[4j + s] in byte j (j = 0..3): the order in which (packed_word >> 2s) &
+// 0x03030303 presents the weights of that group.
+__device__ __forceinline__ uint4 permute_group(uint4 a) {
+  const uint32_t t0 = __byte_perm(a.x, a.y, 0x5140);
+  const uint32_t t1 = __byte_perm(a.x, a.y, 0x7362);
+  const uint32_t t2 = __byte_perm(a.z, a.w, 0x5140);
+  const uint32_t t3 = __byte_perm(a.z, a.w, 0x7362);
+  uint4 o;
+  o.x = __byte_perm(t0, t2, 0x5410);
+  o.y = __byte_perm(t0, t2, 0x7632);
+  o.z = __byte_perm(t1, t3, 0x5410);
+  o.w = __byte_perm(t1, t3, 0x7632);
+  return o;
+}
+
+__device__ __forceinline__ int byte_sum16(uint4 a) {
+  int s = __dp4a((int)a.x, 0x01010101, 0);
+  s = __dp4a((int)a.y, 0x01010101, s);
+  s = __dp4a((int)a.z, 0x01010101, s);
+  return __dp4a((int)a.w, 0x01010101, s);
+}
+
+}  // namespace tw

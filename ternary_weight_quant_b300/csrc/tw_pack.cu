@@ -1,0 +1,141 @@
+// tw_pack.cu -- absmean ternarisation and 2-bit packing of a weight tensor.
+//
+// Conversion step of the bitnet.cpp CPU tutorial (m.qwbw.cn/news/64613) section 3.2:
+// every weight is absmean-quantised onto {-1, 0, +1}; stored 2 bits per weight
+// (section 1.1; the I2_S format of "BitNet 1 位 LLM 独立推理引擎" 正文 para 4).
+//
+// gamma = (float)(S / (N*K)) where S = sum |W| is accumulated EXACTLY: each |W|
+// is an integer m < 2^24 times 2^(b-1-149), so a 256-bucket histogram of the
+// mantissas by exponent holds the sum without error in any order; one warp then
+// turns the histogram into the correctly rounded double.  The result is
+// therefore the same bit pattern for every grid size.
+//
+// Kernel 1 (absmean_hist): grid-stride float4 loads, per-CTA shared histogram
+//   (two 12-bit limbs per bucket, native 32-bit shared atomics), merged into the
+//   workspace histogram with 64-bit global atomics; the last CTA to arrive
+//   (completion counter, no waiting) computes gamma.
+// Kernel 2 (pack): one thread per 32-bit output word (16 weights, 64 bytes of W).
+#include "tw_common.cuh"
+
+namespace tw {
+
+struct PackWorkspace {
+  unsigned long long hist[256];
+  unsigned int done;
+  unsigned int pad[63];
+};
+static_assert(sizeof(PackWorkspace) == 2304, "workspace layout");
+
+__global__ void __launch_bounds__(512) absmean_hist_kernel(const float4* __restrict__ W4, long long n4,
+                                                           PackWorkspace* ws, float* w_scale,
+                                                           long long nk) {
+  // m (< 2^24) split into two 12-bit limbs summed with native 32-bit shared atomics;
+  // a CTA sees at most 2^20 elements (see the launcher), so each limb sum is < 2^32.
+  __shared__ uint32_t hl[256], hh[256];
+  __shared__ unsigned long long hs[256];
+  __shared__ bool is_last;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) hl[i] = hh[i] = 0u;
+  __syncthreads();
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 v = __ldcs(W4 + i);
+    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t m;
+      int b;
+      f32_bucket(e[j], m, b);
+      if (m) {
+        atomicAdd(&hl[b], m & 0xfffu);
+        atomicAdd(&hh[b], m >> 12);
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    const unsigned long long v = (unsigned long long)hl[i] + ((unsigned long long)hh[i] << 12);
+    if (v) atomicAdd(&ws->hist[i], v);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = (atomicAdd(&ws->done, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) hs[i] = __ldcg(&ws->hist[i]);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const double S = warp_exact_hist_to_double(hs, 256, 1, -149);
+    if (threadIdx.x == 0) *w_scale = (float)(S / (double)nk);
+  }
+}
+
+__device__ __forceinline__ uint32_t ternary_code(float w, float gamma) {
+  // t = clamp(rne(w / gamma), -1, 1); code = t + 1.  gamma == 0 -> t = 0.
+  if (gamma == 0.0f) return 1u;
+  int t = __float2int_rn(__fdiv_rn(w, gamma));
+  t = max(-1, min(1, t));
+  return (uint32_t)(t + 1);
+}
+
+__device__ __forceinline__ uint32_t pack4(float4 v, float gamma) {
+  return ternary_code(v.x, gamma) | (ternary_code(v.y, gamma) << 2) | (ternary_code(v.z, gamma) << 4) |
+         (ternary_code(v.w, gamma) << 6);
+}
+
+// One thread per output word (4 bytes = 16 weights); `nbytes` = N*K/4.  Byte i
+// of the packed tensor holds W[4i .. 4i+3] (rows are contiguous in both).
+__global__ void __launch_bounds__(256) pack_kernel(const float4* __restrict__ W4, long long nbytes,
+                                                   const float* __restrict__ w_scale,
+                                                   uint8_t* __restrict__ packed) {
+  const float gamma = *w_scale;
+  const long long nwords = nbytes / 4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  uint32_t* out = reinterpret_cast<uint32_t*>(packed);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nwords; i += stride) {
+    const float4* src = W4 + 4 * i;
+    const uint32_t b0 = pack4(__ldcs(src + 0), gamma);
+    const uint32_t b1 = pack4(__ldcs(src + 1), gamma);
+    const uint32_t b2 = pack4(__ldcs(src + 2), gamma);
+    const uint32_t b3 = pack4(__ldcs(src + 3), gamma);
+    out[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+  // tail bytes (nbytes % 4), handled by the first threads of block 0
+  if (blockIdx.x == 0) {
+    const long long i = nwords * 4 + threadIdx.x;
+    if (i < nbytes) packed[i] = (uint8_t)pack4(__ldcs(W4 + i), gamma);
+  }
+}
+
+}  // namespace tw
+
+// Host launcher (called from tw_api.cu after argument checks).
+cudaError_t tw_launch_pack(const float* W, long long N, long long K, uint8_t* packed, float* w_scale,
+                           void* workspace, cudaStream_t stream, int num_sms) {
+  using namespace tw;
+  PackWorkspace* ws = static_cast<PackWorkspace*>(workspace);
+  cudaError_t err = cudaMemsetAsync(ws, 0, sizeof(PackWorkspace), stream);
+  if (err != cudaSuccess) return err;
+  const long long n = N * K;
+  const long long n4 = n / 4;
+  // at least 4 CTAs per SM, and enough CTAs that none sees more than 2^20 elements
+  long long blocks = (long long)num_sms * 4;
+  const long long need = (n4 + 512LL * 256 - 1) / (512LL * 256);
+  if (blocks < need) blocks = need;
+  if (blocks > (n4 + 511) / 512) blocks = (n4 + 511) / 512;
+  if (blocks < 1) blocks = 1;
+  absmean_hist_kernel<<<(unsigned)blocks, 512, 0, stream>>>(reinterpret_cast<const float4*>(W), n4, ws,
+                                                            w_scale, n);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const long long nbytes = n / 4;
+  long long pblocks = (nbytes / 4 + 255) / 256;
+  const long long pmax = (long long)num_sms * 8;
+  if (pblocks > pmax) pblocks = pmax;
+  if (pblocks < 1) pblocks = 1;
+  pack_kernel<<<(unsigned)pblocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(W), nbytes, w_scale,
+                                                     packed);
+  return cudaGetLastError();
+}
+
+size_t tw_pack_ws_size() { return sizeof(tw::PackWorkspace); }

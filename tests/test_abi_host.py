@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every entry point that include/*.h declares, and
+reject bad arguments on the host -- before any CUDA call -- with the documented
+status codes.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"TW_API\s+[\w\s\*]+?\b(tw_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def tw():
+    import ternary_weight_quant_b300 as tw
+    return tw
+
+
+def test_header_declares_entry_points():
+    names = _declared_symbols()
+    for expected in ["tw_pack_ternary", "tw_quant_act", "tw_rmsnorm_quant_act", "tw_ternary_gemv",
+                     "tw_ternary_gemm", "tw_ternary_matmul", "tw_quant_gemv", "tw_status_string",
+                     "tw_pack_workspace_bytes", "tw_device_status"]:
+        assert expected in names
+
+
+def test_library_exports_every_declared_symbol(tw):
+    lib = ctypes.CDLL(tw.LIB_PATH)
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_internal_launchers_are_hidden(tw):
+    lib = ctypes.CDLL(tw.LIB_PATH)
+    for internal in ["tw_launch_gemv", "tw_launch_pack", "tw_pack_ws_size", "tw_launch_fused_gemv"]:
+        assert not hasattr(lib, internal)
+
+
+def test_status_strings(tw):
+    lib = tw.lib()
+    for code in range(9):
+        s = lib.tw_status_string(code).decode()
+        assert s.startswith("TW_")
+    assert lib.tw_status_string(99).decode() == "unknown tw_status"
+    assert lib.tw_version() >= 100
+
+
+def test_workspace_bytes(tw):
+    assert tw.tw_pack_workspace_bytes(256, 256) >= 256 * 8 + 4
+    assert tw.tw_pack_workspace_bytes(0, 256) == 0
+    assert tw.tw_pack_workspace_bytes(4, 6) == 0
+    assert tw.tw_pack_workspace_bytes(1 << 30, 1 << 12) == 0  # N*K >= 2^40
+
+
+FAKE = 0x10000  # a 64 KiB-aligned non-null address; never dereferenced: these calls fail on the host
+
+
+def test_null_pointers_rejected(tw):
+    lib = tw.lib()
+    assert lib.tw_pack_ternary(None, 4, 4, FAKE, FAKE, FAKE, 4096, None) == tw.TW_ERR_NULL
+    assert lib.tw_quant_act(FAKE, 1, 16, None, FAKE, None, None) == tw.TW_ERR_NULL
+    assert lib.tw_rmsnorm_quant_act(FAKE, None, 1e-6, 1, 16, FAKE, FAKE, None, None) == tw.TW_ERR_NULL
+    for fn in (lib.tw_ternary_gemv, lib.tw_ternary_gemm, lib.tw_ternary_matmul):
+        assert fn(FAKE, FAKE, None, FAKE, None, 1, 4, 16, FAKE, None, None) == tw.TW_ERR_NULL
+        assert fn(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 16, None, None, None) == tw.TW_ERR_NULL
+    assert lib.tw_quant_gemv(None, None, 1e-6, FAKE, FAKE, 1, 4, 64, FAKE, None, None, None, None,
+                             None) == tw.TW_ERR_NULL
+    assert lib.tw_device_status(None) == tw.TW_ERR_NULL
+
+
+@pytest.mark.parametrize("M,N,K", [(0, 4, 16), (1, 0, 16), (1, 4, 0), (1, 4, 6), (1, 4, 65536),
+                                   (-1, 4, 16), (1, 1 << 31, 16)])
+def test_bad_shapes_rejected(tw, M, N, K):
+    lib = tw.lib()
+    for fn in (lib.tw_ternary_gemv, lib.tw_ternary_gemm, lib.tw_ternary_matmul):
+        assert fn(FAKE, FAKE, FAKE, FAKE, None, M, N, K, FAKE, None, None) == tw.TW_ERR_SHAPE
+
+
+def test_gemv_rejects_large_m(tw):
+    lib = tw.lib()
+    assert lib.tw_ternary_gemv(FAKE, FAKE, FAKE, FAKE, None, 17, 4, 16, FAKE, None, None) == tw.TW_ERR_SHAPE
+
+
+def test_quant_gemv_shape_checks(tw):
+    lib = tw.lib()
+    args = lambda M, K: (FAKE, None, 1e-6, FAKE, FAKE, M, 8, K, FAKE, None, None, None, None, None)
+    assert lib.tw_quant_gemv(*args(5, 64)) == tw.TW_ERR_SHAPE     # M > 4
+    assert lib.tw_quant_gemv(*args(1, 80)) == tw.TW_ERR_SHAPE     # K % 64 != 0
+    assert lib.tw_quant_gemv(*args(1, 0)) == tw.TW_ERR_SHAPE
+    bad = (FAKE + 4, None, 1e-6, FAKE, FAKE, 1, 8, 64, FAKE, None, None, None, None, None)
+    assert lib.tw_quant_gemv(*bad) == tw.TW_ERR_ALIGN
+
+
+def test_gemm_requires_k_multiple_of_16(tw):
+    lib = tw.lib()
+    assert lib.tw_ternary_gemm(FAKE, FAKE, FAKE, FAKE, None, 64, 4, 20, FAKE, None, None) == tw.TW_ERR_SHAPE
+
+
+def test_pack_checks(tw):
+    lib = tw.lib()
+    ws = tw.tw_pack_workspace_bytes(4, 16)
+    assert lib.tw_pack_ternary(FAKE, 4, 18, FAKE, FAKE, FAKE, ws, None) == tw.TW_ERR_SHAPE
+    assert lib.tw_pack_ternary(FAKE, 4, 16, FAKE, FAKE, None, ws, None) == tw.TW_ERR_WORKSPACE
+    assert lib.tw_pack_ternary(FAKE, 4, 16, FAKE, FAKE, FAKE, ws - 1, None) == tw.TW_ERR_WORKSPACE
+    assert lib.tw_pack_ternary(FAKE + 4, 4, 16, FAKE, FAKE, FAKE, ws, None) == tw.TW_ERR_ALIGN
+    assert lib.tw_pack_ternary(FAKE, 4, 16, FAKE + 1, FAKE, FAKE, ws, None) == tw.TW_ERR_ALIGN
+
+
+def test_alignment_checks(tw):
+    lib = tw.lib()
+    assert lib.tw_quant_act(FAKE + 8, 1, 16, FAKE, FAKE, None, None) == tw.TW_ERR_ALIGN
+    assert lib.tw_quant_act(FAKE, 1, 16, FAKE + 2, FAKE, None, None) == tw.TW_ERR_ALIGN
+    assert lib.tw_rmsnorm_quant_act(FAKE, FAKE + 4, 1e-6, 1, 16, FAKE, FAKE, None, None) == tw.TW_ERR_ALIGN
+    assert lib.tw_ternary_gemv(FAKE, FAKE + 1, FAKE, FAKE, None, 1, 4, 16, FAKE, None, None) == tw.TW_ERR_ALIGN
+    assert lib.tw_ternary_gemv(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 16, FAKE + 2, None, None) == tw.TW_ERR_ALIGN
+    assert lib.tw_ternary_gemm(FAKE, FAKE, FAKE + 4, FAKE, None, 64, 4, 16, FAKE, None, None) == tw.TW_ERR_ALIGN
