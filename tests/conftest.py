@@ -10,6 +10,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a)")
+    # Build libtw.so (nvcc cross-compiles for sm_103a without a GPU) and the oracle
+    # if they are missing or older than their sources.
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    import oracle
+    oracle.build()
 
 
 def pytest_collection_modifyitems(config, items):
