@@ -34,6 +34,7 @@ cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, cons
                                  float* s_x_out, int32_t* x_sum_out, int32_t* acc_out, cudaStream_t stream,
                                  int num_sms, bool pdl);
 cudaError_t tw_read_stream_status(int* out);
+cudaError_t tw_read_gemm_status(int* out);
 cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
                            int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream, int num_sms,
                            int* unsupported);
@@ -257,12 +258,12 @@ TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, 
 
 TW_API tw_status tw_device_status(int32_t* status) {
   if (!status) return TW_ERR_NULL;
-  int v = 0;
-  if (tw_read_stream_status(&v) != cudaSuccess) {
+  int v = 0, g = 0;
+  if (tw_read_stream_status(&v) != cudaSuccess || tw_read_gemm_status(&g) != cudaSuccess) {
     cudaGetLastError();
     return TW_ERR_CUDA;
   }
-  *status = v;
+  *status = v ? v : g;
   return TW_OK;
 }
 

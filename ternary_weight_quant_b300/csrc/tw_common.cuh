@@ -88,6 +88,20 @@ __device__ __forceinline__ double warp_exact_hist_to_double(const unsigned long 
   return ldexp((double)m, msb - 52 + lsb_exp);
 }
 
+// Dequantisation scale fl(fl(gamma * s_x) / 127) of one token.
+__device__ __forceinline__ float dequant_scale(float gamma, float s_x) {
+  return __fdiv_rn(__fmul_rn(gamma, s_x), 127.0f);
+}
+
+// y = acc * gamma * s_x / 127 as fp32.  With a normal scale c = dequant_scale(): one
+// more rounding, fl(acc * c), within 3 roundings (< 2e-7 relative) of the exact value.
+// When c is subnormal or zero the fp32 chain would lose precision, so the product is
+// formed in double as ((acc * gamma) * s_x) / 127 and rounded once to fp32.
+__device__ __forceinline__ float dequant(int acc, float c, float gamma, float s_x) {
+  if (c >= 1.17549435e-38f) return __fmul_rn((float)acc, c);
+  return (float)((((double)acc * (double)gamma) * (double)s_x) / 127.0);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -1,11 +1,504 @@
-// tw_gemm.cu -- tensor-core (tcgen05) ternary GEMM for larger token batches.
+// tw_gemm.cu -- ternary x int8 product for larger token batches on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// The product is a sign check and an add per weight (bitnet.cpp CPU tutorial,
+// m.qwbw.cn/news/64613, section 1.1); for many tokens it is a dense contraction,
+// so ternary weights are widened for the accumulation ("1-bit 大模型官方推理框架"
+// page, FAQ 2) and fed to the tensor cores:
+//   * weights {-1, 0, +1} and int8 activations are exact in bf16, and every partial
+//     sum of the fp32 accumulation is an integer of magnitude <= 128*K < 2^24, so
+//     the bf16 MMA with fp32 accumulation (kind::f16) yields the exact int32 dot
+//     product in any summation order;
+//   * the tile is "swapped": the MMA's M side (128 lanes of tensor memory) is 128
+//     weight rows and its N side is up to 256 tokens, so batches from 16 tokens up
+//     fill the tensor core without padding the weight side;
+//   * four producer warps read the 2-bit packed weights and the int8 activations
+//     from global memory, widen them to bf16 in registers (the weights with two
+//     byte-permutes per four codes) and store them into shared memory in the
+//     128-byte-swizzled K-major layout the MMA reads; a fifth warp allocates
+//     tensor memory and issues tcgen05.mma from one thread; stages are handed over
+//     with mbarriers (producers -> MMA: thread arrivals; MMA -> producers:
+//     tcgen05.commit);
+//   * within each group of 16 k the widened weights are stored in the order
+//     0,4,1,5,2,6,3,7,8,12,9,13,10,14,11,15 (what the byte permutes produce) and the
+//     activations are stored in the same order, so the dot product is unchanged;
+//   * K may be split across a cluster of CTAs (thread-block cluster along K); each
+//     CTA leaves its partial accumulators in its shared memory and the CTAs of the
+//     cluster sum them through distributed shared memory, each finishing a slice of
+//     the tokens -- no global scratch;
+//   * epilogue: tcgen05.ld of the accumulators, exact conversion to int32, then
+//     y = acc * fl(fl(gamma * s_x) / 127) (the same roundings as the GEMV, dequant()).
+// Every mbarrier wait is bounded (2 s); a CTA that gives up records TW_ERR_TIMEOUT in a
+// device status word, waits (bounded) for the MMAs it issued, frees its tensor
+// memory and returns.
 #include "tw_common.cuh"
+
+namespace tw {
+namespace gemm {
+
+__device__ int g_gemm_status;  // 0 or TW_ERR_TIMEOUT (sticky until read)
+
+constexpr int BM = 128;            // weight rows per CTA (MMA M)
+constexpr int BK = 64;             // k per stage: one 128-byte swizzle row of bf16
+constexpr int kProducers = 128;    // threads of warps 0-3
+constexpr int kThreads = 160;      // + warp 4 (TMEM allocation, MMA issue)
+constexpr int kMaxStages = 8;
+constexpr int kMaxCluster = 8;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+
+struct Args {
+  const uint8_t* packed;
+  const float* w_scale;
+  const int8_t* x_q;
+  const float* s_x;
+  int M, N, K;
+  int BN;          // tokens per CTA tile (multiple of 16, <= 256)
+  int nstages;
+  int ksplit;      // CTAs of a cluster along K (1 = no split)
+  int kstages_per_split;
+  uint32_t ctrl_off;  // byte offset of the barriers after the stage / partials area
+  uint32_t tmem_cols;
+  float* y;
+  int32_t* acc_out;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait (kTimeoutNs of wall time); with abort_flag it also gives up as soon as
+// another role of the CTA has aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag = nullptr) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (abort_flag && *abort_flag) return false;
+      const uint64_t t = global_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > kTimeoutNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)1 << 16;                     // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;                     // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// 16 packed codes (one 32-bit word, k = 0..15) -> 16 bf16 in the order
+// 0,4,1,5,2,6,3,7 | 8,12,9,13,10,14,11,15.  Selector byte b of s is c*0x11 + 0x40:
+// nibble c picks the low bf16 byte from T0, nibble c + 4 the high byte from T1.
+__device__ __forceinline__ void widen_codes(uint32_t w, uint4& lo, uint4& hi) {
+  const uint32_t T0 = 0x00800080u;  // low bytes of bf16(-1), bf16(0), bf16(+1)
+  const uint32_t T1 = 0x003F00BFu;  // high bytes
+  uint32_t o[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t s = ((w >> (2 * j)) & 0x03030303u) * 0x11u + 0x40404040u;
+    o[j] = __byte_perm(T0, T1, s);
+    o[4 + j] = __byte_perm(T0, T1, s >> 16);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_s8(uint32_t w, int i) {
+  const float a = (float)(int)(int8_t)(w >> (8 * i));
+  const float b = (float)(int)(int8_t)(w >> (8 * (i + 1)));
+  return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);  // exact: small integers
+}
+
+// 16 int8 activations (k = 0..15) -> 16 bf16 in the same order as widen_codes.
+__device__ __forceinline__ void widen_acts(uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w0 = __byte_perm(v.x, v.y, 0x5140);  // x0 x4 x1 x5
+  const uint32_t w1 = __byte_perm(v.x, v.y, 0x7362);  // x2 x6 x3 x7
+  const uint32_t w2 = __byte_perm(v.z, v.w, 0x5140);
+  const uint32_t w3 = __byte_perm(v.z, v.w, 0x7362);
+  lo = make_uint4(bf16x2_s8(w0, 0), bf16x2_s8(w0, 2), bf16x2_s8(w1, 0), bf16x2_s8(w1, 2));
+  hi = make_uint4(bf16x2_s8(w2, 0), bf16x2_s8(w2, 2), bf16x2_s8(w3, 0), bf16x2_s8(w3, 2));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
+  extern __shared__ unsigned char smem_raw[];
+  // 1024-byte alignment for the swizzled tiles
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  const int BN = a.BN, NS = a.nstages;
+  const uint32_t b_stage_bytes = (uint32_t)BN * BK * 2;
+  const uint32_t stage_bytes = A_STAGE_BYTES + b_stage_bytes;
+  // control block after the stages (or the split-K partials, whichever is larger)
+  unsigned char* ctrl = gbase + a.ctrl_off;
+  const uint32_t bar_full = smem_u32(ctrl);        // [NS]
+  const uint32_t bar_empty = bar_full + 8 * kMaxStages;  // [NS]
+  const uint32_t bar_done = bar_empty + 8 * kMaxStages;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctrl + 16 * kMaxStages + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 16 * kMaxStages + 12);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = a.ksplit > 1 ? cluster_ctarank() : 0u;
+  const int n0 = blockIdx.x / a.ksplit * BM;  // clusters are consecutive blocks along x
+  const int m0 = blockIdx.y * BN;
+  const int kst0 = (int)crank * a.kstages_per_split;
+  const int nkst_total = (a.K + BK - 1) / BK;
+  const int nk = max(0, min(a.kstages_per_split, nkst_total - kst0));
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_full + 8 * s, kProducers);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 4) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32((const void*)tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ producers
+    const int K = a.K, Kw = K >> 4;  // 32-bit packed words per row
+    const int r = tid;               // weight row of this thread within the tile
+    const int n = n0 + r;
+    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(a.packed) + (size_t)(n < a.N ? n : 0) * Kw;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % NS;
+      const int kw0 = (kst0 + i) * (BK / 16);  // first packed word of this stage
+      // global loads first, then wait for the stage to be free
+      uint32_t pw[4];
+      if (n < a.N && kw0 + 4 <= Kw && (Kw & 3) == 0) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(wrow + kw0));
+        pw[0] = v.x; pw[1] = v.y; pw[2] = v.z; pw[3] = v.w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) pw[q] = (n < a.N && kw0 + q < Kw) ? __ldg(wrow + kw0 + q) : 0x55555555u;
+      }
+      const int bunits = BN * 4;  // 16-byte units of int8 activations in the stage
+      if (i >= NS) {
+        if (!mbar_wait(bar_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+      }
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      const uint32_t As = base + (uint32_t)s * stage_bytes;
+      const uint32_t Bs = As + A_STAGE_BYTES;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 lo, hi;
+        widen_codes(pw[q], lo, hi);  // 0x55555555 = sixteen zero codes
+        st_shared_v4(As + sw128_off(r, 2 * q), lo);
+        st_shared_v4(As + sw128_off(r, 2 * q + 1), hi);
+      }
+      for (int u = tid; u < bunits; u += kProducers) {
+        const int j = u >> 2, q = u & 3;
+        const int m = m0 + j;
+        const int k = (kw0 + q) * 16;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (m < a.M && k < K) v = __ldg(reinterpret_cast<const uint4*>(a.x_q + (size_t)m * K + k));
+        uint4 lo, hi;
+        widen_acts(v, lo, hi);
+        st_shared_v4(Bs + sw128_off(j, 2 * q), lo);
+        st_shared_v4(Bs + sw128_off(j, 2 * q + 1), hi);
+      }
+      fence_async_smem();
+      mbar_arrive(bar_full + 8 * s);
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issue (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BN);
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % NS;
+        if (!mbar_wait(bar_full + 8 * s, (uint32_t)((i / NS) & 1), abort_flag) || *abort_flag) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t As = base + (uint32_t)s * stage_bytes;
+        const uint32_t Bs = As + A_STAGE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          mma_bf16(tmem, sw128_desc(As + 32 * kk), sw128_desc(Bs + 32 * kk), idesc, (i | kk) ? 1u : 0u);
+        }
+        mma_commit(bar_empty + 8 * s);
+        ++issued;
+      }
+      (void)issued;
+      mma_commit(bar_done);  // arrives once every MMA issued above has completed
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ epilogue
+  // All threads wait until the accumulators are final (or the MMAs issued before an
+  // abort have drained), so tensor memory is never freed under a running MMA.
+  const bool done_ok = mbar_wait(bar_done, 0);
+  tc_fence_after();
+  __syncthreads();
+  const bool failed = !done_ok || *abort_flag != 0 || !ok;
+  const int any_fail = __syncthreads_or(failed ? 1 : 0);
+  int cluster_fail = any_fail;
+  float* part = reinterpret_cast<float*>(gbase);  // [BN][BM] partial accumulators (stages are free now)
+  if (a.ksplit > 1) {
+    // publish this CTA's failure state and partials, then combine across the cluster
+    if (warp < 4 && !any_fail) {
+      for (int c0 = 0; c0 < BN; c0 += 8) {
+        uint32_t v[8];
+        if (nk > 0) {
+          tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) v[t] = 0u;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) part[(size_t)(c0 + t) * BM + tid] = __uint_as_float(v[t]);
+      }
+    }
+    if (tid == 0) *abort_flag = any_fail;
+    cluster_sync();
+    for (int rk = 0; rk < a.ksplit; ++rk)
+      cluster_fail |= *static_cast<volatile int*>(__cluster_map_shared_rank((void*)abort_flag, (unsigned)rk));
+    if (!cluster_fail) {
+      // CTA crank finishes tokens [t0, t1) of the tile for all 128 rows; that slice is
+      // contiguous in every CTA's [BN][BM] partials, read 4 floats at a time
+      const int per = (((BN + a.ksplit - 1) / a.ksplit) + 7) & ~7;
+      const int t0 = min(BN, (int)crank * per), t1 = min(BN, t0 + per);
+      const float gam = *a.w_scale;
+      const float4* src[kMaxCluster];
+#pragma unroll
+      for (int rk = 0; rk < kMaxCluster; ++rk)
+        src[rk] = static_cast<const float4*>(
+            __cluster_map_shared_rank((void*)(part + (size_t)t0 * BM), (unsigned)(rk < a.ksplit ? rk : 0)));
+      const int nvec = (t1 - t0) * BM / 4;
+      for (int e = tid; e < nvec; e += kThreads) {
+        int4 acc = make_int4(0, 0, 0, 0);
+#pragma unroll
+        for (int rk = 0; rk < kMaxCluster; ++rk) {
+          if (rk < a.ksplit) {
+            const float4 v = src[rk][e];
+            acc.x += __float2int_rn(v.x); acc.y += __float2int_rn(v.y);
+            acc.z += __float2int_rn(v.z); acc.w += __float2int_rn(v.w);
+          }
+        }
+        const int j = t0 + (4 * e) / BM, rr = (4 * e) % BM;
+        const int m = m0 + j;
+        if (m < a.M) {
+          const float sm = a.s_x[m];
+          const float c = dequant_scale(gam, sm);
+          const int av[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int n = n0 + rr + t;
+            if (n < a.N) {
+              a.y[(size_t)m * a.N + n] = dequant(av[t], c, gam, sm);
+              if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = av[t];
+            }
+          }
+        }
+      }
+    }
+    cluster_sync();  // no CTA leaves while others still read its shared memory
+  } else if (warp < 4 && !any_fail) {
+    const float gam = *a.w_scale;
+    const int n = n0 + tid;
+    for (int c0 = 0; c0 < BN; c0 += 8) {
+      uint32_t v[8];
+      tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int m = m0 + c0 + t;
+        if (m < a.M && n < a.N) {
+          const int acc = __float2int_rn(__uint_as_float(v[t]));
+          const float sm = a.s_x[m];
+          a.y[(size_t)m * a.N + n] = dequant(acc, dequant_scale(gam, sm), gam, sm);
+          if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = acc;
+        }
+      }
+    }
+  }
+  if (tid == 0 && cluster_fail) atomicExch(&g_gemm_status, (int)TW_ERR_TIMEOUT);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
+}  // namespace gemm
+}  // namespace tw
+
+namespace {
+
+struct GemmPlan {
+  int BN, nstages, ksplit, kstages_per_split, tiles_n, tiles_m;
+  uint32_t tmem_cols, ctrl_off;
+  size_t smem;
+};
+
+// Tokens per tile: M rounded up to 16, at most 256; K split over a cluster so that
+// the grid comes close to one CTA per SM without slicing K below 8 stages.
+bool gemm_plan(int M, int N, int K, int num_sms, GemmPlan& p) {
+  using namespace tw::gemm;
+  p.BN = ((M + 15) / 16) * 16;
+  if (p.BN > 256) p.BN = 256;
+  p.tiles_n = (N + BM - 1) / BM;
+  p.tiles_m = (M + p.BN - 1) / p.BN;
+  const int nkst = (K + BK - 1) / BK;
+  const long long tiles = (long long)p.tiles_n * p.tiles_m;
+  p.ksplit = 1;
+  while (p.ksplit < kMaxCluster && tiles * (p.ksplit * 2) <= num_sms && nkst / (p.ksplit * 2) >= 8) p.ksplit *= 2;
+  p.kstages_per_split = (nkst + p.ksplit - 1) / p.ksplit;
+  const size_t stage = (size_t)A_STAGE_BYTES + (size_t)p.BN * BK * 2;
+  const size_t budget = 200 * 1024;
+  p.nstages = (int)(budget / stage);
+  if (p.nstages > kMaxStages) p.nstages = kMaxStages;
+  if (p.nstages > p.kstages_per_split) p.nstages = p.kstages_per_split < 2 ? 2 : p.kstages_per_split;
+  if (p.nstages < 2) return false;
+  // the partial accumulators of a split reuse the stage memory: BN x 128 fp32
+  size_t body = (size_t)p.nstages * stage;
+  const size_t partial = (size_t)p.BN * BM * 4;
+  if (p.ksplit > 1 && body < partial) body = partial;
+  p.ctrl_off = (uint32_t)body;
+  p.smem = 1024 + body + 16 * kMaxStages + 16;
+  // at least 114 KB so that one CTA runs per SM: its tensor memory (<= 256 of the 512
+  // columns) can then always be allocated, also next to a CTA of a concurrent launch
+  if (p.smem < 114 * 1024) p.smem = 114 * 1024;
+  p.tmem_cols = 32;
+  while ((int)p.tmem_cols < p.BN) p.tmem_cols <<= 1;
+  return p.smem <= 227 * 1024;
+}
+
+}  // namespace
 
 cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
                            int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream, int num_sms,
                            int* unsupported) {
-  (void)packed; (void)w_scale; (void)x_q; (void)s_x; (void)M; (void)N; (void)K; (void)y; (void)acc_out;
-  (void)stream; (void)num_sms;
-  *unsupported = 1;
-  return cudaSuccess;
+  using namespace tw::gemm;
+  *unsupported = 0;
+  GemmPlan p;
+  if (K % 16 != 0 || !gemm_plan(M, N, K, num_sms, p)) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  Args a = {};
+  a.packed = packed; a.w_scale = w_scale; a.x_q = x_q; a.s_x = s_x;
+  a.M = M; a.N = N; a.K = K; a.BN = p.BN; a.nstages = p.nstages; a.ksplit = p.ksplit;
+  a.kstages_per_split = p.kstages_per_split; a.tmem_cols = p.tmem_cols; a.ctrl_off = p.ctrl_off; a.y = y; a.acc_out = acc_out;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.tiles_n * p.ksplit), (unsigned)p.tiles_m);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.ksplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, a);
+}
+
+// Reads and clears the GEMM's device status word (synchronous; diagnostics only).
+cudaError_t tw_read_gemm_status(int* out) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, tw::gemm::g_gemm_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(tw::gemm::g_gemm_status, &zero, sizeof(int));
 }

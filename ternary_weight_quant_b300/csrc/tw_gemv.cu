@@ -17,7 +17,7 @@
 // per lane per row are loaded before any is used, so 4*U loads are in flight per
 // lane.  Partial sums are reduced with redux.sync and kept per row in shared
 // memory across K chunks (a chunk is the part of x_q that fits in shared memory
-// for all tokens).  Epilogue: y = (float)acc * fl(fl(gamma * s_x) / 127).
+// for all tokens).  Epilogue: y = (float)acc * fl(fl(gamma * s_x) / 127) (dequant()).
 #include "tw_common.cuh"
 
 namespace tw {
@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(256) gemv_dp4a_kernel(const uint32_t* __restri
     const int m = i / rows, r = i - m * rows;
     const int xsm = need_sum ? xsum_s[m] : x_sum[m];
     const int a = part[r * MT + m] - xsm;
-    const float c = __fdiv_rn(__fmul_rn(gam, s_x[m]), 127.0f);
-    y[(size_t)m * N + row0 + r] = __fmul_rn((float)a, c);
+    const float sm = s_x[m];
+    y[(size_t)m * N + row0 + r] = dequant(a, dequant_scale(gam, sm), gam, sm);
     if (acc_out) acc_out[(size_t)m * N + row0 + r] = a;
   }
 }
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const uint8_t* __rest
     }
     acc = warp_sum(acc);
     if (lane == 0) {
-      const float c = __fdiv_rn(__fmul_rn(gam, s_x[m]), 127.0f);
-      y[(size_t)m * N + n] = __fmul_rn((float)acc, c);
+      const float sm = s_x[m];
+      y[(size_t)m * N + n] = dequant(acc, dequant_scale(gam, sm), gam, sm);
       if (acc_out) acc_out[(size_t)m * N + n] = acc;
     }
   }

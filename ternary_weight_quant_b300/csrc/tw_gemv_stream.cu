@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(StreamArgs a) {
   const float gam = *a.w_scale;
   float cm[MT];
 #pragma unroll
-  for (int m = 0; m < MT; ++m) cm[m] = __fdiv_rn(__fmul_rn(gam, s_scale[m]), 127.0f);
+  for (int m = 0; m < MT; ++m) cm[m] = dequant_scale(gam, s_scale[m]);
 
   // ---------------------------------------------------------------- weight chunks
   for (int ch = 0; ch < nchunks; ++ch) {
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(StreamArgs a) {
         if (lane == m && m < a.M) {
           if (S == 1) {
             const size_t o = (size_t)m * a.N + row0 + crow0 + r;
-            a.y[o] = __fmul_rn((float)tot, cm[m]);
+            a.y[o] = dequant(tot, cm[m], gam, s_scale[m]);
             if (a.acc_out) a.acc_out[o] = tot;
           } else {
             part[(r * S + sl) * MT + m] = tot;
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads) gemv_stream_kernel(StreamArgs a) {
         int tot = 0;
         for (int s2 = 0; s2 < S; ++s2) tot += part[(r * S + s2) * MT + m];
         const size_t o = (size_t)m * a.N + row0 + crow0 + r;
-        a.y[o] = __fmul_rn((float)tot, cm[m]);
+        a.y[o] = dequant(tot, cm[m], gam, s_scale[m]);
         if (a.acc_out) a.acc_out[o] = tot;
       }
       __syncthreads();
