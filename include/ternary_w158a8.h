@@ -119,6 +119,27 @@ TW_API tw_status tw_pack_ternary(const float *W, int64_t N, int64_t K, uint8_t *
                                  tw_stream_t stream);
 
 /*
+ * tw_pack_ternary without a workspace argument, for callers that cannot allocate
+ * device memory at the point of the call: a plug-in running inside a host
+ * framework that owns every device allocation, a service whose memory pools are
+ * fixed at start-up, or a loop that must not allocate after initialisation.  The
+ * pages have no counterpart of this call; it is a convenience of this library.
+ *   Arguments, requirements, results and errors as tw_pack_ternary (minus the
+ *   workspace), so N*K < TW_MAX_NK is the size limit (TW_ERR_SHAPE beyond it).
+ *   Scratch: a 2304-byte array in the library's device memory (a file-scope
+ *   __device__ variable), which every GPU that loads the library holds until the
+ *   process exits.  The call allocates nothing, frees nothing and calls no
+ *   allocating routine; it clears the scratch on `stream` before use.
+ *   The first call on a device looks up the scratch address (cudaGetSymbolAddress,
+ *   with that device current); make that first call before any stream capture.
+ *   All calls share the one scratch array per device: calls whose work overlaps on
+ *   the GPU (different streams, or other threads) race on it and may produce a wrong
+ *   w_scale.  Serialise them, e.g. on one stream.
+ */
+TW_API tw_status tw_pack_ternary_noalloc(const float *W, int64_t N, int64_t K, uint8_t *packed,
+                                         float *w_scale, tw_stream_t stream);
+
+/*
  * Per-token absmax int8 activation quantisation ("BitNet-rs" page, 技术实现细节).
  *   x      [M][K] fp32, 16-byte aligned.
  *   x_q    [M][K] int8 output, 4-byte aligned.

@@ -41,6 +41,7 @@ def _load():
         "tw_version": ([], ctypes.c_int),
         "tw_pack_workspace_bytes": ([i64, i64], sz),
         "tw_pack_ternary": ([p, i64, i64, p, p, p, sz, p], ctypes.c_int),
+        "tw_pack_ternary_noalloc": ([p, i64, i64, p, p, p], ctypes.c_int),
         "tw_quant_act": ([p, i64, i64, p, p, p, p], ctypes.c_int),
         "tw_rmsnorm_quant_act": ([p, p, ctypes.c_float, i64, i64, p, p, p, p], ctypes.c_int),
         "tw_ternary_gemv": ([p, p, p, p, p, i64, i64, i64, p, p, p], ctypes.c_int),
@@ -97,6 +98,16 @@ def tw_pack_ternary(W, packed, w_scale, workspace, N=None, K=None, stream=None):
     ws_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
     _call("tw_pack_ternary", _ptr(W), N, K, _ptr(packed), _ptr(w_scale), _ptr(workspace), ws_bytes,
           _stream(stream))
+
+
+def tw_pack_ternary_noalloc(W, packed, w_scale, N=None, K=None, stream=None):
+    """tw_pack_ternary with the library's own device scratch (no workspace argument).
+
+    For callers that cannot allocate device memory when they pack; calls that overlap
+    on the GPU share one scratch array and must be serialised."""
+    N = W.shape[0] if N is None else N
+    K = W.shape[1] if K is None else K
+    _call("tw_pack_ternary_noalloc", _ptr(W), N, K, _ptr(packed), _ptr(w_scale), _stream(stream))
 
 
 def tw_quant_act(x, x_q, s_x, x_sum=None, M=None, K=None, stream=None):

@@ -15,6 +15,8 @@
 cudaError_t tw_launch_pack(const float* W, long long N, long long K, uint8_t* packed, float* w_scale,
                            void* workspace, cudaStream_t stream, int num_sms);
 size_t tw_pack_ws_size();
+cudaError_t tw_pack_scratch_address(void** out);
+size_t tw_pack_scratch_bytes();
 cudaError_t tw_launch_quant_act(const float* x, long long M, long long K, int8_t* x_q, float* s_x,
                                 int32_t* x_sum, cudaStream_t stream);
 cudaError_t tw_launch_rmsnorm_quant_act(const float* x, const float* g, float eps, long long M, long long K,
@@ -147,6 +149,25 @@ TW_API tw_status tw_pack_ternary(const float* W, int64_t N, int64_t K, uint8_t* 
   st = check_device_ptrs(W, packed, w_scale, static_cast<const uint8_t*>(workspace));
   if (st != TW_OK) return st;
   return from_cuda(tw_launch_pack(W, N, K, packed, w_scale, workspace, (cudaStream_t)stream, sms));
+}
+
+TW_API tw_status tw_pack_ternary_noalloc(const float* W, int64_t N, int64_t K, uint8_t* packed,
+                                         float* w_scale, tw_stream_t stream) {
+  if (!W || !packed || !w_scale) return TW_ERR_NULL;
+  if (N < 1 || check_kdim(K) != TW_OK || N * K >= TW_MAX_NK) return TW_ERR_SHAPE;
+  if (tw_pack_scratch_bytes() < tw_pack_ws_size()) return TW_ERR_WORKSPACE;
+  if (!aligned(W, 16) || !aligned(packed, 4) || !aligned(w_scale, 4)) return TW_ERR_ALIGN;
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(W, packed, w_scale);
+  if (st != TW_OK) return st;
+  void* scratch = nullptr;
+  if (tw_pack_scratch_address(&scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return TW_ERR_CUDA;
+  }
+  return from_cuda(tw_launch_pack(W, N, K, packed, w_scale, scratch, (cudaStream_t)stream, sms));
 }
 
 TW_API tw_status tw_quant_act(const float* x, int64_t M, int64_t K, int8_t* x_q, float* s_x, int32_t* x_sum,

@@ -15,6 +15,8 @@
 //   workspace histogram with 64-bit global atomics; the last CTA to arrive
 //   (completion counter, no waiting) computes gamma.
 // Kernel 2 (pack): one thread per 32-bit output word (16 weights, 64 bytes of W).
+#include <atomic>
+
 #include "tw_common.cuh"
 
 namespace tw {
@@ -139,3 +141,44 @@ cudaError_t tw_launch_pack(const float* W, long long N, long long K, uint8_t* pa
 }
 
 size_t tw_pack_ws_size() { return sizeof(tw::PackWorkspace); }
+
+// ----------------------------------------------------------------------------
+// Allocation-free variant: the same two kernels with their scratch in a
+// file-scope device array instead of a caller-provided workspace.
+//
+// Some callers cannot allocate device memory when they convert weights (a
+// plug-in inside a host framework that owns every device allocation, a service
+// whose memory pools are fixed at start-up, a loop that forbids allocation after
+// initialisation); they pass only the tensors.  The scratch is one histogram plus
+// a completion counter (sizeof(PackWorkspace) = 2304 bytes); every GPU that
+// loads the library keeps it until the process exits.
+namespace {
+
+static __device__ __align__(256) tw::PackWorkspace g_pack_scratch;
+
+constexpr int kMaxScratchDevices = 64;
+std::atomic<uintptr_t> g_pack_scratch_addr[kMaxScratchDevices];  // device address, 0 = not set up
+
+}  // namespace
+
+// Device address of g_pack_scratch on the current device.  The first call on a
+// device looks it up with cudaGetSymbolAddress (in host code the symbol names a
+// host-side stand-in, never the device memory itself); later calls reuse it.
+cudaError_t tw_pack_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+  uintptr_t v = g_pack_scratch_addr[dev].load(std::memory_order_acquire);
+  if (v == 0) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pack_scratch);
+    if (e != cudaSuccess) return e;
+    v = reinterpret_cast<uintptr_t>(p);
+    g_pack_scratch_addr[dev].store(v, std::memory_order_release);
+  }
+  *out = reinterpret_cast<void*>(v);
+  return cudaSuccess;
+}
+
+size_t tw_pack_scratch_bytes() { return sizeof(g_pack_scratch); }
