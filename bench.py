@@ -468,6 +468,62 @@ def run_ours(args):
     return 0
 
 
+def run_kernel_case(args):
+    """One kernel in isolation (for timing sweeps and small ncu captures; not the contract line).
+
+    --kernel-case {gemv,fused,fused_rms,quant,rms_quant,gemm} on --shape NxK at --M tokens, over
+    --copies distinct weight tensors (so the stream leaves L2), each launched --reps times."""
+    import torch
+    import seeded_inputs as si
+    torch.cuda.set_device(0)
+    import ternary_weight_quant_b300 as tw
+    N, K = (int(v) for v in args.shape.lower().split("x"))
+    M = args.M
+    ws = torch.empty(tw.tw_pack_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    packs = []
+    for c in range(args.copies):
+        W = si.device_normal((N, K), seed=77 + c)
+        p = torch.empty((N, K // 4), dtype=torch.uint8, device="cuda")
+        g = torch.empty(1, dtype=torch.float32, device="cuda")
+        tw.tw_pack_ternary(W, p, g, ws)
+        del W
+        packs.append((p, g))
+    x = si.device_normal((M, K), seed=5)
+    gain = 1.0 + 0.1 * si.device_normal((K,), seed=6)
+    xq, sx, xs = tw.quantize(x)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    k = args.kernel_case
+
+    def launch(p, g):
+        if k == "gemv":
+            tw.tw_ternary_gemv(p, g, xq, sx, y, xs)
+        elif k in ("fused", "fused_rms"):
+            tw.tw_quant_gemv(x, p, g, y, g=gain if k == "fused_rms" else None)
+        elif k == "quant":
+            tw.tw_quant_act(x, xq, sx, xs)
+        elif k == "rms_quant":
+            tw.tw_rmsnorm_quant_act(x, gain, 1e-6, xq, sx, xs)
+        elif k == "gemm":
+            tw.tw_ternary_gemm(p, g, xq, sx, y)
+        else:
+            raise SystemExit(f"unknown kernel case {k}")
+
+    for p, g in packs:  # warm-up
+        launch(p, g)
+    torch.cuda.synchronize()
+    a, b = events_new(), events_new()
+    a.record()
+    for _ in range(args.reps):
+        for p, g in packs:
+            launch(p, g)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (args.reps * len(packs))
+    print(json.dumps({"kernel_case": k, "N": N, "K": K, "M": M, "us_per_launch": us,
+                      "GB/s": gemv_bytes(N, K, M) / us / 1e3, "TFLOP/s": 2 * M * N * K / us / 1e6}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,7 +533,15 @@ def main():
     ap.add_argument("--separate", action="store_true", help="quantisation as separate kernels")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-case", default=None,
+                    help="time one kernel alone: gemv, fused, fused_rms, quant, rms_quant or gemm")
+    ap.add_argument("--shape", default="13824x2560", help="NxK for --kernel-case")
+    ap.add_argument("--M", type=int, default=1, help="tokens for --kernel-case")
+    ap.add_argument("--copies", type=int, default=8, help="distinct weight tensors for --kernel-case")
+    ap.add_argument("--reps", type=int, default=3, help="passes over the copies for --kernel-case")
     args = ap.parse_args()
+    if args.kernel_case:
+        return run_kernel_case(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

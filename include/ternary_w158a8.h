@@ -198,7 +198,8 @@ TW_API tw_status tw_ternary_gemv(const uint8_t *packed, const float *w_scale, co
  * finished, and reads x (and writes every output) only after it has.  So the
  * packed weights must not be written by the kernel enqueued immediately before
  * this call on `stream` (weights packed at load time, with any later
- * synchronisation or any other kernel in between, are fine).
+ * synchronisation or any other kernel in between, are fine).  The same holds for
+ * w_scale, which is also read before that point.
  */
 TW_API tw_status tw_quant_gemv(const float *x, const float *g, float eps, const uint8_t *packed,
                                const float *w_scale, int64_t M, int64_t N, int64_t K, float *y,

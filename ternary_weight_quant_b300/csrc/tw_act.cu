@@ -3,8 +3,9 @@
 // Activations are quantised to 8 bit ("BitNet-rs" page, 技术实现细节); the RMSNorm
 // kernel that precedes the ternary GEMV is named on the "1bit-systems" page
 // (技术架构).  Per token m (one CTA each):
-//   [RMSNorm] r = exact sum of x^2 (histogram of 48-bit squared mantissas per
-//             exponent, turned into the correctly rounded double by one warp),
+//   [RMSNorm] r = exact sum of x^2 (128-bit fixed point relative to the row's
+//             largest exponent; rows with a wider exponent spread use a histogram
+//             of 48-bit squared mantissas per exponent), rounded once to double,
 //             ms = (float)(r / K), inv = 1 / sqrt(ms + eps) (IEEE fp32 sqrt and
 //             divide), u = fl(fl(x * inv) * g);
 //   a = max |u|;  x_q = clamp(rne(fl(fl(u * 127) / a)), -128, 127);  s_x = a;
@@ -31,38 +32,82 @@ __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict_
   __shared__ unsigned long long hist[RMS ? 256 : 1];
   __shared__ float red_f[32];
   __shared__ int red_i[32];
+  __shared__ uint32_t red_u[32];
+  __shared__ unsigned long long red_lo[32], red_hi[32];
   __shared__ float sh_inv, sh_amax;
 
   float inv = 1.0f;
   if (RMS) {
-    for (int i = tid; i < 256; i += blockDim.x) limb[0][i] = limb[1][i] = limb[2][i] = 0u;
-    __syncthreads();
+    // E = largest biased exponent of the row (from the largest magnitude's bits)
+    uint32_t mx = 0u;
     for (int i = tid; i < K4; i += blockDim.x) {
       const float4 v = xr[i];
-      const float e[4] = {v.x, v.y, v.z, v.w};
+      mx = max(mx, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                       max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) red_u[warp] = mx;
+    __syncthreads();
+    mx = 0u;
+    for (int w = 0; w < nwarps; ++w) mx = max(mx, red_u[w]);
+    const int E = max((int)(mx >> 23), 1);
+    // exact sum of squares in 128-bit fixed point (fast path)
+    Sum128 sq;
+    sq.lo = sq.hi = 0ull;
+    bool wide = false;
+    for (int i = tid; i < K4; i += blockDim.x) {
+      const float4 v = xr[i];
+      sum128_add_square(sq, v.x, E, wide);
+      sum128_add_square(sq, v.y, E, wide);
+      sum128_add_square(sq, v.z, E, wide);
+      sum128_add_square(sq, v.w, E, wide);
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t mm;
-        int b;
-        f32_bucket(e[j], mm, b);
-        if (mm) {
-          const unsigned long long sq = (unsigned long long)mm * mm;
-          atomicAdd(&limb[0][b], (uint32_t)(sq & 0xffffu));
-          atomicAdd(&limb[1][b], (uint32_t)((sq >> 16) & 0xffffu));
-          atomicAdd(&limb[2][b], (uint32_t)(sq >> 32));
-        }
-      }
+    for (int o = 16; o > 0; o >>= 1) {
+      const Sum128 t = sum128_shfl_xor(sq, o);
+      sum128_add(sq, t.lo, t.hi);
+    }
+    const int any_wide = __syncthreads_or(wide ? 1 : 0);
+    if (lane == 0) {
+      red_lo[warp] = sq.lo;
+      red_hi[warp] = sq.hi;
     }
     __syncthreads();
-    for (int i = tid; i < 256; i += blockDim.x)
-      hist[i] = (unsigned long long)limb[0][i] + ((unsigned long long)limb[1][i] << 16) +
-                ((unsigned long long)limb[2][i] << 32);
-    __syncthreads();
-    if (warp == 0) {
-      const double r = warp_exact_hist_to_double(hist, 256, 2, -298);
-      if (lane == 0) {
-        const float ms = (float)(r / (double)K);
-        sh_inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    if (!any_wide) {
+      if (tid == 0) {
+        Sum128 t;
+        t.lo = t.hi = 0ull;
+        for (int w = 0; w < nwarps; ++w) sum128_add(t, red_lo[w], red_hi[w]);
+        sh_inv = rms_inv(sum128_to_double(t, E), K, eps);
+      }
+    } else {
+      // exponents spread too far for 128 bits: exact exponent-bucket histogram
+      for (int i = tid; i < 256; i += blockDim.x) limb[0][i] = limb[1][i] = limb[2][i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < K4; i += blockDim.x) {
+        const float4 v = xr[i];
+        const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t mm;
+          int b;
+          f32_bucket(e[j], mm, b);
+          if (mm) {
+            const unsigned long long q = (unsigned long long)mm * mm;
+            atomicAdd(&limb[0][b], (uint32_t)(q & 0xffffu));
+            atomicAdd(&limb[1][b], (uint32_t)((q >> 16) & 0xffffu));
+            atomicAdd(&limb[2][b], (uint32_t)(q >> 32));
+          }
+        }
+      }
+      __syncthreads();
+      for (int i = tid; i < 256; i += blockDim.x)
+        hist[i] = (unsigned long long)limb[0][i] + ((unsigned long long)limb[1][i] << 16) +
+                  ((unsigned long long)limb[2][i] << 32);
+      __syncthreads();
+      if (warp == 0) {
+        const double r = warp_exact_hist_to_double(hist, 256, 2, -298);
+        if (lane == 0) sh_inv = rms_inv(r, K, eps);
       }
     }
     __syncthreads();
@@ -94,6 +139,7 @@ __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict_
   a = sh_amax;
 
   // pass: quantise, store, sum
+  const float ra = a > 0.0f ? __frcp_rn(a) : 0.0f;
   int sum = 0;
   char4* out = reinterpret_cast<char4*>(x_q + (size_t)m * K);
   for (int i = tid; i < K4; i += blockDim.x) {
@@ -105,7 +151,7 @@ __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict_
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       int t = 0;
-      if (a > 0.0f) t = __float2int_rn(__fdiv_rn(__fmul_rn(u[j], 127.0f), a));
+      if (a > 0.0f) t = quant_div(__fmul_rn(u[j], 127.0f), a, ra);
       q[j] = max(-128, min(127, t));
       sum += q[j];
     }

@@ -102,6 +102,84 @@ __device__ __forceinline__ float dequant(int acc, float c, float gamma, float s_
   return (float)((((double)acc * (double)gamma) * (double)s_x) / 127.0);
 }
 
+// ---------------------------------------------------------------------------
+// Exact sum of squares of an fp32 row, fast path.
+//
+// |x| = m * 2^(b - 150) with m < 2^24 an integer and b = max(biased exponent, 1).
+// With E the largest b of the row, x^2 = m^2 * 2^(64 - 2(E - b)) units of
+// 2^(2E - 364).  When every nonzero element has E - b <= 32, each term is an
+// integer below 2^112 in those units and K < 2^16 terms fit in 128 bits, so the
+// sum is exact; sq_round() then rounds it once to double.  Rows with a wider
+// exponent spread set `wide` and must take an exact slow path instead.
+struct Sum128 {
+  unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ void sum128_add(Sum128& s, unsigned long long lo, unsigned long long hi) {
+  const unsigned long long t = s.lo + lo;
+  s.hi += hi + (t < s.lo ? 1ull : 0ull);
+  s.lo = t;
+}
+
+// Adds v^2 to s, with E the row's largest biased exponent (max(e, 1)).
+__device__ __forceinline__ void sum128_add_square(Sum128& s, float v, int E, bool& wide) {
+  const uint32_t bits = __float_as_uint(v) & 0x7fffffffu;
+  const uint32_t e8 = bits >> 23;
+  const uint32_t m = e8 ? ((bits & 0x7fffffu) | 0x800000u) : (bits & 0x7fffffu);
+  const int d = E - (e8 ? (int)e8 : 1);
+  wide |= (m != 0u) & (d > 32);
+  const unsigned long long m2 = (d > 32) ? 0ull : (unsigned long long)m * m;  // < 2^48
+  const unsigned __int128 t = (unsigned __int128)m2 << (64 - 2 * min(d, 32));  // shift 0..64
+  sum128_add(s, (unsigned long long)t, (unsigned long long)(t >> 64));
+}
+
+__device__ __forceinline__ Sum128 sum128_shfl_xor(const Sum128& s, int o) {
+  Sum128 r;
+  r.lo = __shfl_xor_sync(0xffffffffu, s.lo, o);
+  r.hi = __shfl_xor_sync(0xffffffffu, s.hi, o);
+  return r;
+}
+
+// (hi * 2^64 + lo) * 2^(2E - 364), rounded once to the nearest double (ties to even).
+// The result is always a normal double (its exponent is at least -362), so it is
+// assembled from its bits: a 53-bit significand m in [2^52, 2^53] is added to the
+// biased exponent field minus one, which also carries m = 2^53 into the exponent.
+__device__ __forceinline__ double sum128_to_double(const Sum128& s, int E) {
+  if (s.hi == 0ull && s.lo == 0ull) return 0.0;
+  const unsigned __int128 v = ((unsigned __int128)s.hi << 64) | s.lo;
+  const int n = s.hi ? 128 - __clzll((long long)s.hi) : 64 - __clzll((long long)s.lo);  // bit length
+  unsigned long long m;
+  if (n <= 53) {
+    m = (unsigned long long)v << (53 - n);
+  } else {
+    const int drop = n - 53;
+    m = (unsigned long long)(v >> drop);
+    const unsigned __int128 rem = v & (((unsigned __int128)1 << drop) - 1);
+    const unsigned __int128 half = (unsigned __int128)1 << (drop - 1);
+    if (rem > half || (rem == half && (m & 1ull))) m += 1ull;
+  }
+  const long long eb = (long long)(n - 1 + 2 * E - 364) + 1023;  // biased exponent of the leading bit
+  return __longlong_as_double((long long)(((unsigned long long)(eb - 1) << 52) + m));
+}
+
+// 1 / sqrt(fl32(r / K) + eps) with IEEE fp32 square root and divide; r / K in double.
+__device__ __forceinline__ float rms_inv(double r, int K, float eps) {
+  const float ms = __double2float_rn(__ddiv_rn(r, (double)K));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// round_half_even(fl32(p / a)) for a > 0 and |p| <= fl32(127 a), the same integer as
+// __float2int_rn(__fdiv_rn(p, a)), with ra = fl32(1 / a).  d = fl(p * ra) is within
+// |p/a| * 2^-22.9 < 1.6e-5 of the exact quotient and fl32(p/a) within 2^-18 of it, so
+// when d is more than 1e-4 away from a half-integer both round to the same integer
+// (rintf(d)); only nearer than that is the exact IEEE divide taken.
+__device__ __forceinline__ int quant_div(float p, float a, float ra) {
+  const float d = __fmul_rn(p, ra);
+  const float r = rintf(d);
+  if (fabsf(d - r) < 0.4999f) return (int)r;
+  return __float2int_rn(__fdiv_rn(p, a));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

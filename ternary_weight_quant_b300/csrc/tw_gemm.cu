@@ -31,6 +31,11 @@
 // Every mbarrier wait is bounded (2 s); a CTA that gives up records TW_ERR_TIMEOUT in a
 // device status word, waits (bounded) for the MMAs it issued, frees its tensor
 // memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
 #include "tw_common.cuh"
 
 namespace tw {
@@ -46,6 +51,7 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxCluster = 8;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr int kMaxBUnits = 256 * 4 / kProducers;  // 16-byte activation units per producer thread
 
 struct Args {
   const uint8_t* packed;
@@ -192,6 +198,102 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Epilogue shared by the GEMM kernels.  Warps 0 .. EPI-1 read the accumulators (warp
+// w may only address tensor-memory lanes 32 (w % 4) .. +31; with 8 warps the two
+// halves of the token columns go to warps w and w + 4).  Without a K split they
+// dequantise and store y directly; with one, every CTA of the cluster leaves its
+// partials in its own shared memory and finishes a slice of the tokens from all of
+// them through distributed shared memory.  Called by all NTHR threads of the CTA.
+template <int EPI, int NTHR>
+__device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* part, volatile int* abort_flag,
+                                         int any_fail, int nk, int n0, int m0, uint32_t crank) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BN = a.BN;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int cols = BN / (EPI / 4), c_begin = half * cols;
+  const int row = quarter * 32 + lane;
+  const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+  int cluster_fail = any_fail;
+  if (a.ksplit > 1) {
+    // publish this CTA's failure state and partials, then combine across the cluster
+    if (warp < EPI && !any_fail) {
+      for (int c0 = c_begin; c0 < c_begin + cols; c0 += 8) {
+        uint32_t v[8];
+        if (nk > 0) {
+          tmem_ld8(taddr + (uint32_t)c0, v);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) v[t] = 0u;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) part[(size_t)(c0 + t) * BM + row] = __uint_as_float(v[t]);
+      }
+    }
+    if (tid == 0) *abort_flag = any_fail;
+    cluster_sync();
+    for (int rk = 0; rk < a.ksplit; ++rk)
+      cluster_fail |= *static_cast<volatile int*>(__cluster_map_shared_rank((void*)abort_flag, (unsigned)rk));
+    if (!cluster_fail) {
+      // CTA crank finishes tokens [t0, t1) of the tile for all 128 rows; that slice is
+      // contiguous in every CTA's [BN][BM] partials, read 4 floats at a time
+      const int per = (((BN + a.ksplit - 1) / a.ksplit) + 7) & ~7;
+      const int t0 = min(BN, (int)crank * per), t1 = min(BN, t0 + per);
+      const float gam = *a.w_scale;
+      const float4* src[kMaxCluster];
+#pragma unroll
+      for (int rk = 0; rk < kMaxCluster; ++rk)
+        src[rk] = static_cast<const float4*>(
+            __cluster_map_shared_rank((void*)(part + (size_t)t0 * BM), (unsigned)(rk < a.ksplit ? rk : 0)));
+      const int nvec = (t1 - t0) * BM / 4;
+      for (int e = tid; e < nvec; e += NTHR) {
+        int4 acc = make_int4(0, 0, 0, 0);
+#pragma unroll
+        for (int rk = 0; rk < kMaxCluster; ++rk) {
+          if (rk < a.ksplit) {
+            const float4 v = src[rk][e];
+            acc.x += __float2int_rn(v.x); acc.y += __float2int_rn(v.y);
+            acc.z += __float2int_rn(v.z); acc.w += __float2int_rn(v.w);
+          }
+        }
+        const int j = t0 + (4 * e) / BM, rr = (4 * e) % BM;
+        const int m = m0 + j;
+        if (m < a.M) {
+          const float sm = a.s_x[m];
+          const float c = dequant_scale(gam, sm);
+          const int av[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int n = n0 + rr + t;
+            if (n < a.N) {
+              a.y[(size_t)m * a.N + n] = dequant(av[t], c, gam, sm);
+              if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = av[t];
+            }
+          }
+        }
+      }
+    }
+    cluster_sync();  // no CTA leaves while others still read its shared memory
+  } else if (warp < EPI && !any_fail) {
+    const float gam = *a.w_scale;
+    const int n = n0 + row;
+    for (int c0 = c_begin; c0 < c_begin + cols; c0 += 8) {
+      uint32_t v[8];
+      tmem_ld8(taddr + (uint32_t)c0, v);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int m = m0 + c0 + t;
+        if (m < a.M && n < a.N) {
+          const int acc = __float2int_rn(__uint_as_float(v[t]));
+          const float sm = a.s_x[m];
+          a.y[(size_t)m * a.N + n] = dequant(acc, dequant_scale(gam, sm), gam, sm);
+          if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = acc;
+        }
+      }
+    }
+  }
+  if (tid == 0 && cluster_fail) atomicExch(&g_gemm_status, (int)TW_ERR_TIMEOUT);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
   extern __shared__ unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled tiles
@@ -241,23 +343,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
 
   if (warp < 4) {
     // ------------------------------------------------------------ producers
+    // Each thread owns weight row r of the tile and BN/32 16-byte units of the
+    // activations per stage.  The global loads of stage i+1 are issued before
+    // stage i is widened and stored, so their latency overlaps that work.
     const int K = a.K, Kw = K >> 4;  // 32-bit packed words per row
     const int r = tid;               // weight row of this thread within the tile
     const int n = n0 + r;
     const uint32_t* wrow = reinterpret_cast<const uint32_t*>(a.packed) + (size_t)(n < a.N ? n : 0) * Kw;
-    for (int i = 0; i < nk; ++i) {
-      const int s = i % NS;
-      const int kw0 = (kst0 + i) * (BK / 16);  // first packed word of this stage
-      // global loads first, then wait for the stage to be free
-      uint32_t pw[4];
-      if (n < a.N && kw0 + 4 <= Kw && (Kw & 3) == 0) {
+    const int bunits = BN * 4;       // 16-byte units of int8 activations per stage
+    const bool vec_ok = (Kw & 3) == 0;
+    auto load_stage = [&](int i, uint32_t (&pw)[4], uint4 (&bv)[kMaxBUnits]) {
+      const int kw0 = (kst0 + i) * (BK / 16);
+      if (n < a.N && vec_ok && kw0 + 4 <= Kw) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(wrow + kw0));
         pw[0] = v.x; pw[1] = v.y; pw[2] = v.z; pw[3] = v.w;
       } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) pw[q] = (n < a.N && kw0 + q < Kw) ? __ldg(wrow + kw0 + q) : 0x55555555u;
       }
-      const int bunits = BN * 4;  // 16-byte units of int8 activations in the stage
+#pragma unroll
+      for (int t = 0; t < kMaxBUnits; ++t) {
+        const int u = tid + t * kProducers;
+        bv[t] = make_uint4(0u, 0u, 0u, 0u);
+        if (u < bunits) {
+          const int m = m0 + (u >> 2), k = (kw0 + (u & 3)) * 16;
+          if (m < a.M && k < K) bv[t] = __ldg(reinterpret_cast<const uint4*>(a.x_q + (size_t)m * K + k));
+        }
+      }
+    };
+    uint32_t pw[4];
+    uint4 bv[kMaxBUnits];
+    if (nk > 0) load_stage(0, pw, bv);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % NS;
+      uint32_t pw_n[4];
+      uint4 bv_n[kMaxBUnits];
+      if (i + 1 < nk) load_stage(i + 1, pw_n, bv_n);
       if (i >= NS) {
         if (!mbar_wait(bar_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag)) {
           ok = false;
@@ -278,19 +399,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
         st_shared_v4(As + sw128_off(r, 2 * q), lo);
         st_shared_v4(As + sw128_off(r, 2 * q + 1), hi);
       }
-      for (int u = tid; u < bunits; u += kProducers) {
-        const int j = u >> 2, q = u & 3;
-        const int m = m0 + j;
-        const int k = (kw0 + q) * 16;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (m < a.M && k < K) v = __ldg(reinterpret_cast<const uint4*>(a.x_q + (size_t)m * K + k));
-        uint4 lo, hi;
-        widen_acts(v, lo, hi);
-        st_shared_v4(Bs + sw128_off(j, 2 * q), lo);
-        st_shared_v4(Bs + sw128_off(j, 2 * q + 1), hi);
+#pragma unroll
+      for (int t = 0; t < kMaxBUnits; ++t) {
+        const int u = tid + t * kProducers;
+        if (u < bunits) {
+          const int j = u >> 2, q = u & 3;
+          uint4 lo, hi;
+          widen_acts(bv[t], lo, hi);
+          st_shared_v4(Bs + sw128_off(j, 2 * q), lo);
+          st_shared_v4(Bs + sw128_off(j, 2 * q + 1), hi);
+        }
       }
       fence_async_smem();
       mbar_arrive(bar_full + 8 * s);
+      if (i + 1 < nk) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) pw[q] = pw_n[q];
+#pragma unroll
+        for (int t = 0; t < kMaxBUnits; ++t) bv[t] = bv_n[t];
+      }
     }
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issue (one thread)
@@ -328,90 +455,195 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
   __syncthreads();
   const bool failed = !done_ok || *abort_flag != 0 || !ok;
   const int any_fail = __syncthreads_or(failed ? 1 : 0);
-  int cluster_fail = any_fail;
-  float* part = reinterpret_cast<float*>(gbase);  // [BN][BM] partial accumulators (stages are free now)
-  if (a.ksplit > 1) {
-    // publish this CTA's failure state and partials, then combine across the cluster
-    if (warp < 4 && !any_fail) {
-      for (int c0 = 0; c0 < BN; c0 += 8) {
-        uint32_t v[8];
-        if (nk > 0) {
-          tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 8; ++t) v[t] = 0u;
-        }
-#pragma unroll
-        for (int t = 0; t < 8; ++t) part[(size_t)(c0 + t) * BM + tid] = __uint_as_float(v[t]);
-      }
-    }
-    if (tid == 0) *abort_flag = any_fail;
-    cluster_sync();
-    for (int rk = 0; rk < a.ksplit; ++rk)
-      cluster_fail |= *static_cast<volatile int*>(__cluster_map_shared_rank((void*)abort_flag, (unsigned)rk));
-    if (!cluster_fail) {
-      // CTA crank finishes tokens [t0, t1) of the tile for all 128 rows; that slice is
-      // contiguous in every CTA's [BN][BM] partials, read 4 floats at a time
-      const int per = (((BN + a.ksplit - 1) / a.ksplit) + 7) & ~7;
-      const int t0 = min(BN, (int)crank * per), t1 = min(BN, t0 + per);
-      const float gam = *a.w_scale;
-      const float4* src[kMaxCluster];
-#pragma unroll
-      for (int rk = 0; rk < kMaxCluster; ++rk)
-        src[rk] = static_cast<const float4*>(
-            __cluster_map_shared_rank((void*)(part + (size_t)t0 * BM), (unsigned)(rk < a.ksplit ? rk : 0)));
-      const int nvec = (t1 - t0) * BM / 4;
-      for (int e = tid; e < nvec; e += kThreads) {
-        int4 acc = make_int4(0, 0, 0, 0);
-#pragma unroll
-        for (int rk = 0; rk < kMaxCluster; ++rk) {
-          if (rk < a.ksplit) {
-            const float4 v = src[rk][e];
-            acc.x += __float2int_rn(v.x); acc.y += __float2int_rn(v.y);
-            acc.z += __float2int_rn(v.z); acc.w += __float2int_rn(v.w);
-          }
-        }
-        const int j = t0 + (4 * e) / BM, rr = (4 * e) % BM;
-        const int m = m0 + j;
-        if (m < a.M) {
-          const float sm = a.s_x[m];
-          const float c = dequant_scale(gam, sm);
-          const int av[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int n = n0 + rr + t;
-            if (n < a.N) {
-              a.y[(size_t)m * a.N + n] = dequant(av[t], c, gam, sm);
-              if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = av[t];
-            }
-          }
-        }
-      }
-    }
-    cluster_sync();  // no CTA leaves while others still read its shared memory
-  } else if (warp < 4 && !any_fail) {
-    const float gam = *a.w_scale;
-    const int n = n0 + tid;
-    for (int c0 = 0; c0 < BN; c0 += 8) {
-      uint32_t v[8];
-      tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int m = m0 + c0 + t;
-        if (m < a.M && n < a.N) {
-          const int acc = __float2int_rn(__uint_as_float(v[t]));
-          const float sm = a.s_x[m];
-          a.y[(size_t)m * a.N + n] = dequant(acc, dequant_scale(gam, sm), gam, sm);
-          if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = acc;
-        }
-      }
-    }
-  }
-  if (tid == 0 && cluster_fail) atomicExch(&g_gemm_status, (int)TW_ERR_TIMEOUT);
+  epilogue<4, kThreads>(a, tmem, reinterpret_cast<float*>(gbase), abort_flag, any_fail, nk, n0, m0, crank);
 
   tc_fence_before();
   __syncthreads();
   if (warp == 4) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
+
+// ----------------------------------------------------------------------------
+// TMA-fed variant (K % 64 == 0).  One thread issues 2-D tensor copies
+// (cp.async.bulk.tensor) of the raw tiles -- 128 rows x 16 bytes of packed codes
+// and BN rows x 64 int8 activations per 64-k stage -- into a ring of kRawStages
+// raw stages; eight converter warps widen them from shared memory into the
+// swizzled bf16 operand ring; one thread issues the MMAs.  Global loads thus run
+// several stages ahead of the conversion without holding registers.
+constexpr int kTmaConv = 256;     // converter threads (warps 0-7); also the epilogue
+constexpr int kTmaThreads = 320;  // + warp 8 (tensor copies) + warp 9 (TMEM, MMA)
+constexpr int kRawStages = 4;
+constexpr int A_RAW_BYTES = BM * (BK / 4);  // 2 KB
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    gemm_tma_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, Args a) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw0 = smem_u32(smem_raw);
+  const uint32_t base = (raw0 + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw0);
+  const int BN = a.BN, NS = a.nstages, RS = kRawStages;
+  const uint32_t op_bytes = A_STAGE_BYTES + (uint32_t)BN * BK * 2;   // multiple of 1024
+  const uint32_t rawB_bytes = (uint32_t)BN * BK;                     // int8 activations
+  const uint32_t raw_bytes = A_RAW_BYTES + rawB_bytes;               // multiple of 1024
+  const uint32_t op0 = base, rawbase = base + (uint32_t)NS * op_bytes;
+  unsigned char* ctrl = gbase + a.ctrl_off;
+  const uint32_t raw_full = smem_u32(ctrl);           // [kRawStages]
+  const uint32_t raw_empty = raw_full + 8 * kRawStages;
+  const uint32_t op_full = raw_empty + 8 * kRawStages;  // [kMaxStages]
+  const uint32_t op_empty = op_full + 8 * kMaxStages;
+  const uint32_t bar_done = op_empty + 8 * kMaxStages;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctrl + 16 * kRawStages + 16 * kMaxStages + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 16 * kRawStages + 16 * kMaxStages + 12);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = a.ksplit > 1 ? cluster_ctarank() : 0u;
+  const int n0 = blockIdx.x / a.ksplit * BM;
+  const int m0 = blockIdx.y * BN;
+  const int kst0 = (int)crank * a.kstages_per_split;
+  const int nkst_total = a.K / BK;
+  const int nk = max(0, min(a.kstages_per_split, nkst_total - kst0));
+
+  if (tid == 0) {
+    for (int s = 0; s < RS; ++s) {
+      mbar_init(raw_full + 8 * s, 1);
+      mbar_init(raw_empty + 8 * s, kTmaConv / 32);
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(op_full + 8 * s, kTmaConv);
+      mbar_init(op_empty + 8 * s, 1);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32((const void*)tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ tensor copies
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapB)) : "memory");
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int rs = i % RS;
+        if (i >= RS && !mbar_wait(raw_empty + 8 * rs, (uint32_t)(((i / RS) - 1) & 1), abort_flag)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        const int kb = (kst0 + i) * BK;  // first k of the stage
+        const uint32_t dA = rawbase + (uint32_t)rs * raw_bytes;
+        mbar_arrive_expect_tx(raw_full + 8 * rs, raw_bytes);
+        tma_load_2d(dA, &mapA, kb / 4, n0, raw_full + 8 * rs);
+        tma_load_2d(dA + A_RAW_BYTES, &mapB, kb, m0, raw_full + 8 * rs);
+        issued = i + 1;
+      }
+      // never leave with tensor copies in flight into this CTA's shared memory
+      for (int i = max(0, issued - RS); i < issued; ++i) mbar_wait(raw_full + 8 * (i % RS), (uint32_t)((i / RS) & 1));
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issue (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BN);
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % NS;
+        if (!mbar_wait(op_full + 8 * s, (uint32_t)((i / NS) & 1), abort_flag) || *abort_flag) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t As = op0 + (uint32_t)s * op_bytes;
+        const uint32_t Bs = As + A_STAGE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16(tmem, sw128_desc(As + 32 * kk), sw128_desc(Bs + 32 * kk), idesc, (i | kk) ? 1u : 0u);
+        mma_commit(op_empty + 8 * s);
+      }
+      mma_commit(bar_done);  // arrives once every MMA issued above has completed
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ converters (warps 0-7)
+    const int bunits = BN * 4;  // 16-byte units of raw activations per stage
+    for (int i = 0; i < nk; ++i) {
+      const int rs = i % RS, s = i % NS;
+      if (!mbar_wait(raw_full + 8 * rs, (uint32_t)((i / RS) & 1), abort_flag) ||
+          (i >= NS && !mbar_wait(op_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag))) {
+        ok = false;
+        *abort_flag = 1;
+        break;
+      }
+      const uint32_t rA = rawbase + (uint32_t)rs * raw_bytes, rB = rA + A_RAW_BYTES;
+      const uint32_t As = op0 + (uint32_t)s * op_bytes, Bs = As + A_STAGE_BYTES;
+      {  // weights: thread t widens half a row (2 words = 32 codes) into 4 chunks
+        const int r = tid >> 1, h = tid & 1;
+        uint32_t w0, w1;
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(rA + (uint32_t)(r * 16 + h * 8)));
+        uint4 lo, hi;
+        widen_codes(w0, lo, hi);
+        st_shared_v4(As + sw128_off(r, 4 * h + 0), lo);
+        st_shared_v4(As + sw128_off(r, 4 * h + 1), hi);
+        widen_codes(w1, lo, hi);
+        st_shared_v4(As + sw128_off(r, 4 * h + 2), lo);
+        st_shared_v4(As + sw128_off(r, 4 * h + 3), hi);
+      }
+      for (int u = tid; u < bunits; u += kTmaConv) {  // activations: 16 int8 -> 16 bf16
+        const int j = u >> 2, q = u & 3;
+        uint4 v;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(rB + (uint32_t)(16 * u)));
+        uint4 lo, hi;
+        widen_acts(v, lo, hi);
+        st_shared_v4(Bs + sw128_off(j, 2 * q), lo);
+        st_shared_v4(Bs + sw128_off(j, 2 * q + 1), hi);
+      }
+      fence_async_smem();
+      mbar_arrive(op_full + 8 * s);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(raw_empty + 8 * rs);
+    }
+  }
+
+  // ------------------------------------------------------------ epilogue
+  const bool done_ok = mbar_wait(bar_done, 0);
+  tc_fence_after();
+  __syncthreads();
+  const bool failed = !done_ok || *abort_flag != 0 || !ok;
+  const int any_fail = __syncthreads_or(failed ? 1 : 0);
+  epilogue<8, kTmaThreads>(a, tmem, reinterpret_cast<float*>(gbase), abort_flag, any_fail, nk, n0, m0, crank);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
                  : "memory");
@@ -464,11 +696,96 @@ bool gemm_plan(int M, int N, int K, int num_sms, GemmPlan& p) {
 
 }  // namespace
 
+namespace {
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::atomic<void*> fn{nullptr};
+  void* f = fn.load(std::memory_order_acquire);
+  if (!f) {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    fn.store(f, std::memory_order_release);
+  }
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// 2-D byte tensor [rows][cols] (row stride = cols bytes), tiles of box_rows x box_cols,
+// no swizzle, zero fill outside the tensor.
+bool encode_bytes_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                     uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {cols, rows};
+  cuuint64_t gstride[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Shared memory of the TMA kernel: NS operand stages + 4 raw stages (or the split-K
+// partials, whichever is larger) + barriers; at least 114 KB (one CTA per SM).
+bool gemm_tma_plan(GemmPlan& p) {
+  using namespace tw::gemm;
+  const size_t raw = (size_t)A_RAW_BYTES + (size_t)p.BN * BK;
+  const size_t op = (size_t)A_STAGE_BYTES + (size_t)p.BN * BK * 2;
+  const size_t budget = 200 * 1024 - kRawStages * raw;
+  int ns = (int)(budget / op);
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns > p.kstages_per_split) ns = p.kstages_per_split < 2 ? 2 : p.kstages_per_split;
+  if (ns < 2) return false;
+  p.nstages = ns;
+  size_t body = (size_t)ns * op + kRawStages * raw;
+  const size_t partial = (size_t)p.BN * BM * 4;
+  if (p.ksplit > 1 && body < partial) body = partial;
+  p.ctrl_off = (uint32_t)body;
+  p.smem = 1024 + body + 16 * kRawStages + 16 * kMaxStages + 16;
+  if (p.smem < 114 * 1024) p.smem = 114 * 1024;
+  return p.smem <= 227 * 1024;
+}
+
+}  // namespace
+
 cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
                            int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream, int num_sms,
                            int* unsupported) {
   using namespace tw::gemm;
   *unsupported = 0;
+  if (K % 64 == 0) {
+    GemmPlan p;
+    CUtensorMap mapA, mapB;
+    if (gemm_plan(M, N, K, num_sms, p) && gemm_tma_plan(p) &&
+        encode_bytes_2d(&mapA, packed, (uint64_t)K / 4, (uint64_t)N, BK / 4, BM) &&
+        encode_bytes_2d(&mapB, x_q, (uint64_t)K, (uint64_t)M, BK, (uint32_t)p.BN)) {
+      Args a = {};
+      a.packed = packed; a.w_scale = w_scale; a.x_q = x_q; a.s_x = s_x;
+      a.M = M; a.N = N; a.K = K; a.BN = p.BN; a.nstages = p.nstages; a.ksplit = p.ksplit;
+      a.kstages_per_split = p.kstages_per_split; a.tmem_cols = p.tmem_cols; a.ctrl_off = p.ctrl_off;
+      a.y = y; a.acc_out = acc_out;
+      cudaError_t e = cudaFuncSetAttribute(gemm_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)p.smem);
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(p.tiles_n * p.ksplit), (unsigned)p.tiles_m);
+      cfg.blockDim = dim3(kTmaThreads);
+      cfg.dynamicSmemBytes = p.smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)p.ksplit;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, gemm_tma_kernel, mapA, mapB, a);
+    }
+  }
   GemmPlan p;
   if (K % 16 != 0 || !gemm_plan(M, N, K, num_sms, p)) {
     *unsupported = 1;

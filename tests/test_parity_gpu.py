@@ -151,6 +151,66 @@ def test_act_special_rows(tw):
             assert (host(a).view(np.uint8) == b.view(np.uint8)).all(), use_rms
 
 
+def near_tie_tokens(K=256, M=8, seed=0):
+    """Tokens whose quotients x*127/max|x| sit on, or a few ulps either side of, the
+    half-integers where round-half-even decides (the kernels take a fast reciprocal
+    path away from them and the IEEE divide near them)."""
+    rng = np.random.default_rng(seed)
+    x = np.empty((M, K), np.float32)
+    for m in range(M):
+        a = np.float32(rng.uniform(0.5, 4.0))
+        k = rng.integers(-127, 127, size=K).astype(np.float32) + np.float32(0.5)
+        v = (k * a / np.float32(127.0)).astype(np.float32)
+        steps = rng.integers(-3, 4, size=K)
+        for i in range(K):
+            for _ in range(abs(int(steps[i]))):
+                v[i] = np.nextafter(v[i], np.float32(np.inf) if steps[i] > 0 else np.float32(-np.inf))
+        v[0] = a if m % 2 == 0 else -a
+        x[m] = v
+    return x
+
+
+def test_quant_near_rounding_ties(tw):
+    x = near_tie_tokens()
+    ref = oracle.quant_act(x)
+    got = tw.quantize(dev(x))
+    for a_, b_ in zip(got, ref):
+        assert (host(a_).view(np.uint8) == b_.view(np.uint8)).all()
+    W = si.weights(64, x.shape[1], seed=3)
+    p_ref, g_ref = oracle.pack_ternary(W)
+    for m0 in (0, 4):
+        xs_ = x[m0:m0 + 4]
+        q_ref, s_ref, _ = oracle.quant_act(xs_)
+        y_ref, acc_ref = oracle.ternary_matmul(p_ref, g_ref, q_ref, s_ref)
+        y, acc, xq, sx, _, _ = fused_run(tw, xs_, p_ref, g_ref, None)
+        assert (xq == q_ref).all() and (acc == acc_ref).all()
+
+
+@pytest.mark.parametrize("spread", [30, 32, 33, 40])
+def test_rmsnorm_exponent_spread_edges(tw, spread):
+    """Rows whose smallest nonzero element is 2^-spread below the largest: up to 2^-32 the
+    kernels sum the squares in 128-bit fixed point, beyond it they take the exponent-bucket
+    path; both must give the oracle's x_q and s_x bit for bit (standalone and fused)."""
+    K, N = 256, 64
+    x = si.activations(3, K, seed=spread)
+    x[:, 0] = 1024.0
+    x[:, 1] = np.float32(1024.0 * 2.0 ** -spread)
+    x[1, 2] = np.float32(1024.0 * 2.0 ** -spread * 1.5)
+    x[2] *= np.float32(2.0 ** -120)          # the same spread near the bottom of the range
+    g = si.rms_gain(K, seed=spread)
+    ref = oracle.rmsnorm_quant_act(x, g, si.RMS_EPS)
+    got = tw.quantize(dev(x), dev(g), si.RMS_EPS)
+    for a_, b_ in zip(got, ref):
+        assert (host(a_).view(np.uint8) == b_.view(np.uint8)).all()
+    W = si.weights(N, K, seed=spread + 1)
+    p_ref, g_ref = oracle.pack_ternary(W)
+    y_ref, acc_ref = oracle.ternary_matmul(p_ref, g_ref, ref[0], ref[1])
+    y, acc, xq, sx, xs, _ = fused_run(tw, x, p_ref, g_ref, g)
+    assert (xq == ref[0]).all() and (sx.view(np.uint32) == ref[1].view(np.uint32)).all()
+    assert (acc == acc_ref).all()
+    assert_y_close(y, y_ref)
+
+
 # ----------------------------------------------------------------------------- GEMV / matmul
 def product_case(M, N, K, seed, outliers=False):
     W, x = si.gemv_case(M, N, K, seed=seed, outliers=outliers)
