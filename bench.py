@@ -472,7 +472,8 @@ def run_kernel_case(args):
     """One kernel in isolation (for timing sweeps and small ncu captures; not the contract line).
 
     --kernel-case {gemv,fused,fused_rms,quant,rms_quant,gemm} on --shape NxK at --M tokens, over
-    --copies distinct weight tensors (so the stream leaves L2), each launched --reps times."""
+    --copies distinct weight tensors (so the stream leaves L2); one pass over them is captured in
+    a CUDA graph and replayed --reps times (device time per launch, host launch cost excluded)."""
     import torch
     import seeded_inputs as si
     torch.cuda.set_device(0)
@@ -492,6 +493,7 @@ def run_kernel_case(args):
     gain = 1.0 + 0.1 * si.device_normal((K,), seed=6)
     xq, sx, xs = tw.quantize(x)
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    gws = tw.gemm_workspace(M, K)
     k = args.kernel_case
 
     def launch(p, g):
@@ -504,18 +506,33 @@ def run_kernel_case(args):
         elif k == "rms_quant":
             tw.tw_rmsnorm_quant_act(x, gain, 1e-6, xq, sx, xs)
         elif k == "gemm":
+            tw.tw_ternary_gemm(p, g, xq, sx, y, workspace=gws)
+        elif k == "gemm_nows":
             tw.tw_ternary_gemm(p, g, xq, sx, y)
         else:
             raise SystemExit(f"unknown kernel case {k}")
 
-    for p, g in packs:  # warm-up
-        launch(p, g)
+    def one_pass():
+        for p, g in packs:
+            launch(p, g)
+
+    # one pass over the copies captured in a CUDA graph, so host launch cost does not show
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        one_pass()  # warm-up (and lazy initialisation) outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        one_pass()
+    for _ in range(3):
+        graph.replay()
     torch.cuda.synchronize()
     a, b = events_new(), events_new()
     a.record()
     for _ in range(args.reps):
-        for p, g in packs:
-            launch(p, g)
+        graph.replay()
     b.record()
     torch.cuda.synchronize()
     us = a.elapsed_time(b) * 1e3 / (args.reps * len(packs))
@@ -534,7 +551,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-case", default=None,
-                    help="time one kernel alone: gemv, fused, fused_rms, quant, rms_quant or gemm")
+                    help="time one kernel alone: gemv, fused, fused_rms, quant, rms_quant, gemm or gemm_nows")
     ap.add_argument("--shape", default="13824x2560", help="NxK for --kernel-case")
     ap.add_argument("--M", type=int, default=1, help="tokens for --kernel-case")
     ap.add_argument("--copies", type=int, default=8, help="distinct weight tensors for --kernel-case")

@@ -207,6 +207,13 @@ TW_API tw_status tw_quant_gemv(const float *x, const float *g, float eps, const 
                                tw_stream_t stream);
 
 /*
+ * Device scratch (bytes) that tw_ternary_gemm / tw_ternary_matmul can use for an M x K
+ * activation block: a bf16 copy of x_q in the tensor cores' K order.  0 for shapes the
+ * calls would reject.
+ */
+TW_API size_t tw_gemm_workspace_bytes(int64_t M, int64_t K);
+
+/*
  * The same product for larger token batches on the tensor cores ("1-bit 大模型官方推理框架"
  * page, FAQ 2: ternary weights restored to a wider type for the accumulation).
  * Weights are unpacked to bf16 {-1, 0, +1} and activations to bf16 integers in
@@ -214,18 +221,32 @@ TW_API tw_status tw_quant_gemv(const float *x, const float *g, float eps, const 
  * every partial sum is an integer below 2^24 (|acc| <= 128 * K).
  * Arguments as tw_ternary_gemv; M >= 1 (any size), K % 16 == 0, packed and x_q
  * 16-byte aligned (other K: TW_ERR_SHAPE).
+ *   workspace  NULL, or device scratch of at least tw_gemm_workspace_bytes(M, K) bytes,
+ *              256-byte aligned (TW_ERR_WORKSPACE / TW_ERR_ALIGN otherwise).  With it, and
+ *              K % 64 == 0, the activations are widened once per call into the scratch
+ *              and the tensor-memory-access unit loads them already in the operand
+ *              layout; without it every CTA widens its own activation tiles (slower).
+ *              Its contents on entry do not matter; it must not be used by other work
+ *              until this call's work on `stream` has finished.
+ * Tiles of 128 weight rows x up to 256 tokens; K is split over a thread-block cluster
+ * (up to 8 CTAs, partial sums combined through distributed shared memory) when the
+ * tile grid alone would leave SMs idle.
  */
 TW_API tw_status tw_ternary_gemm(const uint8_t *packed, const float *w_scale, const int8_t *x_q,
                                  const float *s_x, const int32_t *x_sum, int64_t M, int64_t N,
-                                 int64_t K, float *y, int32_t *acc_out, tw_stream_t stream);
+                                 int64_t K, float *y, int32_t *acc_out, void *workspace,
+                                 size_t ws_bytes, tw_stream_t stream);
 
 /*
- * The product for any M: tw_ternary_gemv below the measured crossover,
- * tw_ternary_gemm above it.  Arguments as tw_ternary_gemv, any M >= 1.
+ * The product for any M: tw_ternary_gemv below the measured crossover (M <= 16),
+ * tw_ternary_gemm above it (when K % 16 == 0 and packed / x_q are 16-byte aligned; an
+ * exact CUDA-core kernel otherwise).  Arguments as tw_ternary_gemm; the workspace is
+ * used only on the tensor-core path and may be NULL.
  */
 TW_API tw_status tw_ternary_matmul(const uint8_t *packed, const float *w_scale, const int8_t *x_q,
                                    const float *s_x, const int32_t *x_sum, int64_t M, int64_t N,
-                                   int64_t K, float *y, int32_t *acc_out, tw_stream_t stream);
+                                   int64_t K, float *y, int32_t *acc_out, void *workspace,
+                                   size_t ws_bytes, tw_stream_t stream);
 
 /*
  * Reads and clears the library's device status word: 0, or TW_ERR_TIMEOUT when a

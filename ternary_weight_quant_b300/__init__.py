@@ -45,8 +45,9 @@ def _load():
         "tw_quant_act": ([p, i64, i64, p, p, p, p], ctypes.c_int),
         "tw_rmsnorm_quant_act": ([p, p, ctypes.c_float, i64, i64, p, p, p, p], ctypes.c_int),
         "tw_ternary_gemv": ([p, p, p, p, p, i64, i64, i64, p, p, p], ctypes.c_int),
-        "tw_ternary_gemm": ([p, p, p, p, p, i64, i64, i64, p, p, p], ctypes.c_int),
-        "tw_ternary_matmul": ([p, p, p, p, p, i64, i64, i64, p, p, p], ctypes.c_int),
+        "tw_ternary_gemm": ([p, p, p, p, p, i64, i64, i64, p, p, p, sz, p], ctypes.c_int),
+        "tw_ternary_matmul": ([p, p, p, p, p, i64, i64, i64, p, p, p, sz, p], ctypes.c_int),
+        "tw_gemm_workspace_bytes": ([i64, i64], sz),
         "tw_quant_gemv": ([p, p, ctypes.c_float, p, p, i64, i64, i64, p, p, p, p, p, p], ctypes.c_int),
         "tw_device_status": ([p], ctypes.c_int),
     }
@@ -136,12 +137,27 @@ def tw_ternary_gemv(packed, w_scale, x_q, s_x, y, x_sum=None, acc_out=None, **kw
     _product("tw_ternary_gemv", packed, w_scale, x_q, s_x, y, x_sum, acc_out, **kw)
 
 
-def tw_ternary_gemm(packed, w_scale, x_q, s_x, y, x_sum=None, acc_out=None, **kw):
-    _product("tw_ternary_gemm", packed, w_scale, x_q, s_x, y, x_sum, acc_out, **kw)
+def tw_gemm_workspace_bytes(M: int, K: int) -> int:
+    return int(_lib.tw_gemm_workspace_bytes(M, K))
 
 
-def tw_ternary_matmul(packed, w_scale, x_q, s_x, y, x_sum=None, acc_out=None, **kw):
-    _product("tw_ternary_matmul", packed, w_scale, x_q, s_x, y, x_sum, acc_out, **kw)
+def _product_ws(name, packed, w_scale, x_q, s_x, y, x_sum=None, acc_out=None, workspace=None, M=None, N=None,
+                K=None, stream=None):
+    M = x_q.shape[0] if M is None else M
+    K = x_q.shape[-1] if K is None else K
+    N = packed.shape[0] if N is None else N
+    ws_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+    _call(name, _ptr(packed), _ptr(w_scale), _ptr(x_q), _ptr(s_x), _ptr(x_sum), M, N, K, _ptr(y),
+          _ptr(acc_out), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def tw_ternary_gemm(packed, w_scale, x_q, s_x, y, x_sum=None, acc_out=None, workspace=None, **kw):
+    """Tensor-core product; workspace (optional, tw_gemm_workspace_bytes(M, K) bytes) speeds it up."""
+    _product_ws("tw_ternary_gemm", packed, w_scale, x_q, s_x, y, x_sum, acc_out, workspace, **kw)
+
+
+def tw_ternary_matmul(packed, w_scale, x_q, s_x, y, x_sum=None, acc_out=None, workspace=None, **kw):
+    _product_ws("tw_ternary_matmul", packed, w_scale, x_q, s_x, y, x_sum, acc_out, workspace, **kw)
 
 
 def tw_quant_gemv(x, packed, w_scale, y, g=None, eps=1e-6, x_q=None, s_x=None, x_sum=None, acc_out=None,
@@ -185,10 +201,15 @@ def quantize(x: torch.Tensor, g: torch.Tensor | None = None, eps: float = 1e-6, 
     return x_q, s_x, x_sum
 
 
-def matmul(packed, w_scale, x_q, s_x, x_sum=None, acc=False, stream=None):
+def gemm_workspace(M: int, K: int, device="cuda"):
+    """Allocate the optional tensor-core workspace for an M x K activation block."""
+    return torch.empty(max(tw_gemm_workspace_bytes(M, K), 256), dtype=torch.uint8, device=device)
+
+
+def matmul(packed, w_scale, x_q, s_x, x_sum=None, acc=False, workspace=None, stream=None):
     """Allocate y (and optionally acc) and run tw_ternary_matmul."""
     M, N = x_q.shape[0], packed.shape[0]
     y = torch.empty((M, N), dtype=torch.float32, device=x_q.device)
     a = torch.empty((M, N), dtype=torch.int32, device=x_q.device) if acc else None
-    tw_ternary_matmul(packed, w_scale, x_q, s_x, y, x_sum, a, stream=stream)
+    tw_ternary_matmul(packed, w_scale, x_q, s_x, y, x_sum, a, workspace=workspace, stream=stream)
     return (y, a) if acc else y

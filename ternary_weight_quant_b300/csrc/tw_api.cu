@@ -38,8 +38,9 @@ cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, cons
 cudaError_t tw_read_stream_status(int* out);
 cudaError_t tw_read_gemm_status(int* out);
 cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
-                           int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream, int num_sms,
-                           int* unsupported);
+                           int M, int N, int K, float* y, int32_t* acc_out, void* workspace, cudaStream_t stream,
+                           int num_sms, int* unsupported);
+size_t tw_gemm_ws_size(long long M, long long K);
 
 namespace {
 
@@ -236,37 +237,48 @@ TW_API tw_status tw_quant_gemv(const float* x, const float* g, float eps, const 
                                         x_sum_out, acc_out, (cudaStream_t)stream, sms, true));
 }
 
+TW_API size_t tw_gemm_workspace_bytes(int64_t M, int64_t K) {
+  if (M < 1 || M > (1LL << 31) - 1 || check_kdim(K) != TW_OK || M * K >= (1LL << 40)) return 0;
+  return tw_gemm_ws_size(M, K);
+}
+
 TW_API tw_status tw_ternary_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
                                  const float* s_x, const int32_t* x_sum, int64_t M, int64_t N, int64_t K,
-                                 float* y, int32_t* acc_out, tw_stream_t stream) {
+                                 float* y, int32_t* acc_out, void* workspace, size_t ws_bytes, tw_stream_t stream) {
   (void)x_sum;
   tw_status st = check_product_args(packed, w_scale, x_q, s_x, M, N, K, y);
   if (st != TW_OK) return st;
   if (K % 16 != 0) return TW_ERR_SHAPE;
-  if (!aligned(x_q, 16) || !aligned(packed, 16) || !aligned(acc_out, 4)) return TW_ERR_ALIGN;
+  if (workspace && ws_bytes < tw_gemm_ws_size(M, K)) return TW_ERR_WORKSPACE;
+  if (!aligned(x_q, 16) || !aligned(packed, 16) || !aligned(acc_out, 4) || !aligned(workspace, 256))
+    return TW_ERR_ALIGN;
   int sms = 0;
   st = device_info(&sms);
   if (st != TW_OK) return st;
-  st = check_device_ptrs(packed, w_scale, x_q, s_x, y, acc_out);
+  st = check_device_ptrs(packed, w_scale, x_q, s_x, y, acc_out, static_cast<const uint8_t*>(workspace));
   if (st != TW_OK) return st;
   int unsupported = 0;
-  cudaError_t e = tw_launch_gemm(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
+  cudaError_t e = tw_launch_gemm(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out, workspace,
                                  (cudaStream_t)stream, sms, &unsupported);
   if (unsupported) return TW_ERR_UNSUPPORTED;
   return from_cuda(e);
 }
 
-// Token count from which the tensor-core GEMM takes over (disabled until the GEMM is enabled).
-static const int64_t kGemmCrossoverM = INT64_MAX;
+// Token count from which the tensor-core GEMM takes over from the GEMV kernels.
+static const int64_t kGemmCrossoverM = 17;
 
 TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
                                    const float* s_x, const int32_t* x_sum, int64_t M, int64_t N, int64_t K,
-                                   float* y, int32_t* acc_out, tw_stream_t stream) {
+                                   float* y, int32_t* acc_out, void* workspace, size_t ws_bytes,
+                                   tw_stream_t stream) {
   tw_status st = check_product_args(packed, w_scale, x_q, s_x, M, N, K, y);
   if (st != TW_OK) return st;
-  if (M <= TW_GEMV_MAX_M) return tw_ternary_gemv(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, stream);
-  if (M >= kGemmCrossoverM && K % 16 == 0 && aligned(x_q, 16) && aligned(packed, 16))
-    return tw_ternary_gemm(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, stream);
+  if (M < kGemmCrossoverM && M <= TW_GEMV_MAX_M)
+    return tw_ternary_gemv(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, stream);
+  if (K % 16 == 0 && aligned(x_q, 16) && aligned(packed, 16))
+    return tw_ternary_gemm(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, workspace, ws_bytes, stream);
+  if (M <= TW_GEMV_MAX_M)
+    return tw_ternary_gemv(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, stream);
   if (!aligned(acc_out, 4)) return TW_ERR_ALIGN;
   int sms = 0;
   st = device_info(&sms);

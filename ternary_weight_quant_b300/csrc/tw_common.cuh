@@ -96,10 +96,18 @@ __device__ __forceinline__ float dequant_scale(float gamma, float s_x) {
 // y = acc * gamma * s_x / 127 as fp32.  With a normal scale c = dequant_scale(): one
 // more rounding, fl(acc * c), within 3 roundings (< 2e-7 relative) of the exact value.
 // When c is subnormal or zero the fp32 chain would lose precision, so the product is
-// formed in double as ((acc * gamma) * s_x) / 127 and rounded once to fp32.
-__device__ __forceinline__ float dequant(int acc, float c, float gamma, float s_x) {
-  if (c >= 1.17549435e-38f) return __fmul_rn((float)acc, c);
+// formed in double as ((acc * gamma) * s_x) / 127 and rounded once to fp32 (a zero
+// gamma or s_x gives the signed zero directly).
+// Out of line, so that the double arithmetic never appears (not even predicated off)
+// in the callers' hot loops: this part's double-precision pipe is narrow.
+static __device__ __noinline__ float dequant_tiny(int acc, float gamma, float s_x) {
+  if (gamma == 0.0f || s_x == 0.0f) return __fmul_rn((float)acc, 0.0f);  // the exact product, signed zero
   return (float)((((double)acc * (double)gamma) * (double)s_x) / 127.0);
+}
+
+__device__ __forceinline__ float dequant(int acc, float c, float gamma, float s_x) {
+  if (__builtin_expect(c >= 1.17549435e-38f, 1)) return __fmul_rn((float)acc, c);
+  return dequant_tiny(acc, gamma, s_x);
 }
 
 // ---------------------------------------------------------------------------

@@ -51,6 +51,8 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxCluster = 8;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr int kScaleOff = 256;                // per-token scales: this far into the control block
+constexpr int kCtrlBytes = kScaleOff + 2 * 256 * 4;
 constexpr int kMaxBUnits = 256 * 4 / kProducers;  // 16-byte activation units per producer thread
 
 struct Args {
@@ -204,15 +206,40 @@ __device__ __forceinline__ void cluster_sync() {
 // dequantise and store y directly; with one, every CTA of the cluster leaves its
 // partials in its own shared memory and finishes a slice of the tokens from all of
 // them through distributed shared memory.  Called by all NTHR threads of the CTA.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Epilogue shared by the GEMM kernels.  Warps 0 .. EPI-1 read the accumulators (warp
+// w may only address tensor-memory lanes 32 (w % 4) .. +31; with 8 warps the two
+// halves of the token columns go to warps w and w + 4).  Without a K split they
+// dequantise and store y directly; with one, every CTA of the cluster leaves its
+// partials in its own shared memory and finishes a slice of the tokens from all of
+// them through distributed shared memory.  Called by all NTHR threads of the CTA;
+// `scale` holds, per token of the tile, s_x and fl(fl(gamma * s_x) / 127)
+// (2 x BN floats, filled before the main loop).
 template <int EPI, int NTHR>
 __device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* part, volatile int* abort_flag,
-                                         int any_fail, int nk, int n0, int m0, uint32_t crank) {
+                                         int any_fail, int nk, int n0, int m0, uint32_t crank,
+                                         const float* scale) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BN = a.BN;
   const int quarter = warp & 3, half = warp >> 2;
   const int cols = BN / (EPI / 4), c_begin = half * cols;
   const int row = quarter * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+  const float gam = __ldg(a.w_scale);
+  const float* sxs = scale;       // [BN] s_x of the tile's tokens
+  const float* cs = scale + BN;   // [BN] dequantisation scales
   int cluster_fail = any_fail;
   if (a.ksplit > 1) {
     // publish this CTA's failure state and partials, then combine across the cluster
@@ -238,7 +265,6 @@ __device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* pa
       // contiguous in every CTA's [BN][BM] partials, read 4 floats at a time
       const int per = (((BN + a.ksplit - 1) / a.ksplit) + 7) & ~7;
       const int t0 = min(BN, (int)crank * per), t1 = min(BN, t0 + per);
-      const float gam = *a.w_scale;
       const float4* src[kMaxCluster];
 #pragma unroll
       for (int rk = 0; rk < kMaxCluster; ++rk)
@@ -258,8 +284,7 @@ __device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* pa
         const int j = t0 + (4 * e) / BM, rr = (4 * e) % BM;
         const int m = m0 + j;
         if (m < a.M) {
-          const float sm = a.s_x[m];
-          const float c = dequant_scale(gam, sm);
+          const float sm = sxs[j], c = cs[j];
           const int av[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
@@ -274,24 +299,49 @@ __device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* pa
     }
     cluster_sync();  // no CTA leaves while others still read its shared memory
   } else if (warp < EPI && !any_fail) {
-    const float gam = *a.w_scale;
     const int n = n0 + row;
-    for (int c0 = c_begin; c0 < c_begin + cols; c0 += 8) {
-      uint32_t v[8];
-      tmem_ld8(taddr + (uint32_t)c0, v);
+    const bool nv = n < a.N;
+    if ((cols & 31) == 0) {
+      for (int c0 = c_begin; c0 < c_begin + cols; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)c0, v);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int m = m0 + c0 + t;
-        if (m < a.M && n < a.N) {
-          const int acc = __float2int_rn(__uint_as_float(v[t]));
-          const float sm = a.s_x[m];
-          a.y[(size_t)m * a.N + n] = dequant(acc, dequant_scale(gam, sm), gam, sm);
-          if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = acc;
+        for (int t = 0; t < 32; ++t) {
+          const int j = c0 + t, m = m0 + j;
+          if (m < a.M && nv) {
+            const int acc = __float2int_rn(__uint_as_float(v[t]));
+            a.y[(size_t)m * a.N + n] = dequant(acc, cs[j], gam, sxs[j]);
+            if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = acc;
+          }
+        }
+      }
+    } else {
+      for (int c0 = c_begin; c0 < c_begin + cols; c0 += 8) {
+        uint32_t v[8];
+        tmem_ld8(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int j = c0 + t, m = m0 + j;
+          if (m < a.M && nv) {
+            const int acc = __float2int_rn(__uint_as_float(v[t]));
+            a.y[(size_t)m * a.N + n] = dequant(acc, cs[j], gam, sxs[j]);
+            if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = acc;
+          }
         }
       }
     }
   }
   if (tid == 0 && cluster_fail) atomicExch(&g_gemm_status, (int)TW_ERR_TIMEOUT);
+}
+
+// Per-token scales of the tile into shared memory (called by `nthr` threads).
+__device__ __forceinline__ void load_scales(const Args& a, int m0, float* scale, int t, int nthr) {
+  const float gam = __ldg(a.w_scale);
+  for (int j = t; j < a.BN; j += nthr) {
+    const float sm = (m0 + j < a.M) ? __ldg(a.s_x + m0 + j) : 0.0f;
+    scale[j] = sm;
+    scale[a.BN + j] = dequant_scale(gam, sm);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
@@ -371,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
         }
       }
     };
+    load_scales(a, m0, reinterpret_cast<float*>(ctrl + kScaleOff), tid, kProducers);
     uint32_t pw[4];
     uint4 bv[kMaxBUnits];
     if (nk > 0) load_stage(0, pw, bv);
@@ -455,7 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
   __syncthreads();
   const bool failed = !done_ok || *abort_flag != 0 || !ok;
   const int any_fail = __syncthreads_or(failed ? 1 : 0);
-  epilogue<4, kThreads>(a, tmem, reinterpret_cast<float*>(gbase), abort_flag, any_fail, nk, n0, m0, crank);
+  epilogue<4, kThreads>(a, tmem, reinterpret_cast<float*>(gbase), abort_flag, any_fail, nk, n0, m0, crank,
+                        reinterpret_cast<const float*>(ctrl + kScaleOff));
 
   tc_fence_before();
   __syncthreads();
@@ -469,15 +521,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
 
 // ----------------------------------------------------------------------------
 // TMA-fed variant (K % 64 == 0).  One thread issues 2-D tensor copies
-// (cp.async.bulk.tensor) of the raw tiles -- 128 rows x 16 bytes of packed codes
-// and BN rows x 64 int8 activations per 64-k stage -- into a ring of kRawStages
-// raw stages; eight converter warps widen them from shared memory into the
-// swizzled bf16 operand ring; one thread issues the MMAs.  Global loads thus run
-// several stages ahead of the conversion without holding registers.
+// (cp.async.bulk.tensor) of the activation tiles: with the workspace, the bf16 copy
+// straight into the operand stage (128-byte swizzle done by the copy engine);
+// without it, raw int8 tiles into a small ring.  The packed weight tile is only 16
+// bytes per row and stage, a poor shape for the copy engine, so each converter
+// thread fetches its own 8 bytes with cp.async, kARing stages ahead, and widens
+// exactly what it fetched.  One thread issues the MMAs.
 constexpr int kTmaConv = 256;     // converter threads (warps 0-7); also the epilogue
 constexpr int kTmaThreads = 320;  // + warp 8 (tensor copies) + warp 9 (TMEM, MMA)
-constexpr int kRawStages = 4;
-constexpr int A_RAW_BYTES = BM * (BK / 4);  // 2 KB
+constexpr int kRawStages = 4;                 // raw int8 activation tiles in flight (no workspace)
+constexpr int A_RAW_BYTES = BM * (BK / 4);    // 2 KB of packed codes per stage
+constexpr int kARing = 8;                     // stages of packed codes in flight (cp.async)
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
@@ -490,6 +544,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// kBPre: the activations were widened beforehand (bf16, MMA K order) and mapB
+// describes that copy with 128-byte swizzle, so its tiles land directly in the
+// operand stage and the converters widen only the weights.
+template <bool kBPre>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     gemm_tma_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, Args a) {
   extern __shared__ unsigned char smem_raw[];
@@ -497,10 +555,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint32_t base = (raw0 + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw0);
   const int BN = a.BN, NS = a.nstages, RS = kRawStages;
+  (void)mapA;
   const uint32_t op_bytes = A_STAGE_BYTES + (uint32_t)BN * BK * 2;   // multiple of 1024
-  const uint32_t rawB_bytes = (uint32_t)BN * BK;                     // int8 activations
-  const uint32_t raw_bytes = A_RAW_BYTES + rawB_bytes;               // multiple of 1024
-  const uint32_t op0 = base, rawbase = base + (uint32_t)NS * op_bytes;
+  const uint32_t raw_bytes = kBPre ? 0u : (uint32_t)BN * BK;         // raw int8 activations
+  const uint32_t op0 = base;
+  const uint32_t araw = base + (uint32_t)NS * op_bytes;              // [kARing][128 rows][16 B]
+  const uint32_t rawbase = araw + (uint32_t)kARing * A_RAW_BYTES;    // [RS][raw_bytes]
   unsigned char* ctrl = gbase + a.ctrl_off;
   const uint32_t raw_full = smem_u32(ctrl);           // [kRawStages]
   const uint32_t raw_empty = raw_full + 8 * kRawStages;
@@ -524,7 +584,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_init(raw_empty + 8 * s, kTmaConv / 32);
     }
     for (int s = 0; s < NS; ++s) {
-      mbar_init(op_full + 8 * s, kTmaConv);
+      mbar_init(op_full + 8 * s, kTmaConv / 32 + (kBPre ? 1 : 0));
       mbar_init(op_empty + 8 * s, 1);
     }
     mbar_init(bar_done, 1);
@@ -547,25 +607,37 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ tensor copies
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapB)) : "memory");
       int issued = 0;
       for (int i = 0; i < nk; ++i) {
-        const int rs = i % RS;
-        if (i >= RS && !mbar_wait(raw_empty + 8 * rs, (uint32_t)(((i / RS) - 1) & 1), abort_flag)) {
-          ok = false;
-          *abort_flag = 1;
-          break;
-        }
         const int kb = (kst0 + i) * BK;  // first k of the stage
-        const uint32_t dA = rawbase + (uint32_t)rs * raw_bytes;
-        mbar_arrive_expect_tx(raw_full + 8 * rs, raw_bytes);
-        tma_load_2d(dA, &mapA, kb / 4, n0, raw_full + 8 * rs);
-        tma_load_2d(dA + A_RAW_BYTES, &mapB, kb, m0, raw_full + 8 * rs);
+        if constexpr (kBPre) {
+          const int s = i % NS;
+          if (i >= NS && !mbar_wait(op_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag)) {
+            ok = false;
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(op_full + 8 * s, (uint32_t)BN * BK * 2);
+          tma_load_2d(op0 + (uint32_t)s * op_bytes + A_STAGE_BYTES, &mapB, kb, m0, op_full + 8 * s);
+        } else {
+          const int rs = i % RS;
+          if (i >= RS && !mbar_wait(raw_empty + 8 * rs, (uint32_t)(((i / RS) - 1) & 1), abort_flag)) {
+            ok = false;
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(raw_full + 8 * rs, raw_bytes);
+          tma_load_2d(rawbase + (uint32_t)rs * raw_bytes, &mapB, kb, m0, raw_full + 8 * rs);
+        }
         issued = i + 1;
       }
       // never leave with tensor copies in flight into this CTA's shared memory
-      for (int i = max(0, issued - RS); i < issued; ++i) mbar_wait(raw_full + 8 * (i % RS), (uint32_t)((i / RS) & 1));
+      if constexpr (kBPre) {
+        for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(op_full + 8 * (i % NS), (uint32_t)((i / NS) & 1));
+      } else {
+        for (int i = max(0, issued - RS); i < issued; ++i) mbar_wait(raw_full + 8 * (i % RS), (uint32_t)((i / RS) & 1));
+      }
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -592,21 +664,46 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ converters (warps 0-7)
+    load_scales(a, m0, reinterpret_cast<float*>(ctrl + kScaleOff), tid, kTmaConv);
     const int bunits = BN * 4;  // 16-byte units of raw activations per stage
+    // thread t owns 8 bytes (32 codes) of weight row t / 2 in every stage
+    const int r = tid >> 1, h = tid & 1;
+    const bool rowv = n0 + r < a.N;
+    const uint8_t* gA = a.packed + (size_t)(rowv ? n0 + r : 0) * (a.K / 4) + h * 8;
+    const uint32_t aslot = araw + (uint32_t)(r * 16 + h * 8);
+    auto fetch = [&](int i) {  // stage i of this CTA -> ring slot i % kARing (one group per stage)
+      if (i < nk && rowv) {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(aslot + (uint32_t)(i % kARing) * A_RAW_BYTES),
+                     "l"(gA + (size_t)(kst0 + i) * (BK / 4))
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+#pragma unroll
+    for (int i = 0; i < kARing; ++i) fetch(i);
     for (int i = 0; i < nk; ++i) {
       const int rs = i % RS, s = i % NS;
-      if (!mbar_wait(raw_full + 8 * rs, (uint32_t)((i / RS) & 1), abort_flag) ||
-          (i >= NS && !mbar_wait(op_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag))) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(kARing - 1) : "memory");  // this thread's stage i
+      int okw = 1;
+      if (lane == 0) {
+        okw = (kBPre || mbar_wait(raw_full + 8 * rs, (uint32_t)((i / RS) & 1), abort_flag)) &&
+              (i < NS || mbar_wait(op_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag));
+      }
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      __syncwarp();
+      if (!okw) {
         ok = false;
         *abort_flag = 1;
         break;
       }
-      const uint32_t rA = rawbase + (uint32_t)rs * raw_bytes, rB = rA + A_RAW_BYTES;
+      const uint32_t rB = rawbase + (uint32_t)rs * raw_bytes;
       const uint32_t As = op0 + (uint32_t)s * op_bytes, Bs = As + A_STAGE_BYTES;
-      {  // weights: thread t widens half a row (2 words = 32 codes) into 4 chunks
-        const int r = tid >> 1, h = tid & 1;
+      {  // weights: widen the 32 codes this thread fetched into 4 chunks of its row
         uint32_t w0, w1;
-        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(rA + (uint32_t)(r * 16 + h * 8)));
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                     : "=r"(w0), "=r"(w1)
+                     : "r"(aslot + (uint32_t)(i % kARing) * A_RAW_BYTES));
+        if (!rowv) w0 = w1 = 0x55555555u;  // rows past N: zero codes (their outputs are dropped)
         uint4 lo, hi;
         widen_codes(w0, lo, hi);
         st_shared_v4(As + sw128_off(r, 4 * h + 0), lo);
@@ -615,7 +712,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         st_shared_v4(As + sw128_off(r, 4 * h + 2), lo);
         st_shared_v4(As + sw128_off(r, 4 * h + 3), hi);
       }
-      for (int u = tid; u < bunits; u += kTmaConv) {  // activations: 16 int8 -> 16 bf16
+      fetch(i + kARing);  // the slot just read is free again
+      for (int u = tid; u < (kBPre ? 0 : bunits); u += kTmaConv) {  // activations: 16 int8 -> 16 bf16
         const int j = u >> 2, q = u & 3;
         uint4 v;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -626,11 +724,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         st_shared_v4(Bs + sw128_off(j, 2 * q), lo);
         st_shared_v4(Bs + sw128_off(j, 2 * q + 1), hi);
       }
-      fence_async_smem();
-      mbar_arrive(op_full + 8 * s);
+      fence_async_smem();  // this thread's operand stores become visible to the tensor cores
       __syncwarp();
-      if (lane == 0) mbar_arrive(raw_empty + 8 * rs);
+      if (lane == 0) {     // one arrival per warp (after all its lanes fenced)
+        mbar_arrive(op_full + 8 * s);
+        if (!kBPre) mbar_arrive(raw_empty + 8 * rs);
+      }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may land after this CTA is gone
   }
 
   // ------------------------------------------------------------ epilogue
@@ -639,7 +740,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   __syncthreads();
   const bool failed = !done_ok || *abort_flag != 0 || !ok;
   const int any_fail = __syncthreads_or(failed ? 1 : 0);
-  epilogue<8, kTmaThreads>(a, tmem, reinterpret_cast<float*>(gbase), abort_flag, any_fail, nk, n0, m0, crank);
+  epilogue<8, kTmaThreads>(a, tmem, reinterpret_cast<float*>(gbase), abort_flag, any_fail, nk, n0, m0, crank,
+                           reinterpret_cast<const float*>(ctrl + kScaleOff));
 
   tc_fence_before();
   __syncthreads();
@@ -648,6 +750,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
                  : "memory");
   }
+}
+
+
+// x_q [M][K] int8 -> bf16 [M][K], each 16-element group in the MMA K order
+// 0,4,1,5,2,6,3,7,8,12,9,13,10,14,11,15 (the order widen_codes gives the weights).
+__global__ void __launch_bounds__(256) widen_acts_kernel(const int8_t* __restrict__ x_q, long long groups,
+                                                         uint4* __restrict__ out) {
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= groups) return;
+  uint4 lo, hi;
+  widen_acts(__ldg(reinterpret_cast<const uint4*>(x_q) + g), lo, hi);
+  out[2 * g] = lo;
+  out[2 * g + 1] = hi;
 }
 
 }  // namespace gemm
@@ -685,7 +800,7 @@ bool gemm_plan(int M, int N, int K, int num_sms, GemmPlan& p) {
   const size_t partial = (size_t)p.BN * BM * 4;
   if (p.ksplit > 1 && body < partial) body = partial;
   p.ctrl_off = (uint32_t)body;
-  p.smem = 1024 + body + 16 * kMaxStages + 16;
+  p.smem = 1024 + body + kCtrlBytes;
   // at least 114 KB so that one CTA runs per SM: its tensor memory (<= 256 of the 512
   // columns) can then always be allocated, also next to a CTA of a concurrent launch
   if (p.smem < 114 * 1024) p.smem = 114 * 1024;
@@ -716,60 +831,81 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D byte tensor [rows][cols] (row stride = cols bytes), tiles of box_rows x box_cols,
 // no swizzle, zero fill outside the tensor.
-bool encode_bytes_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                     uint32_t box_rows) {
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, int esize, const void* base, uint64_t cols,
+               uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t gdim[2] = {cols, rows};
-  cuuint64_t gstride[1] = {cols};
+  cuuint64_t gstride[1] = {cols * (uint64_t)esize};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estride[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estride,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(map, type, 2, const_cast<void*>(base), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D byte tensor [rows][cols] (row stride = cols bytes), no swizzle, zero fill outside.
+bool encode_bytes_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                     uint32_t box_rows) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, cols, rows, box_cols, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Shared memory of the TMA kernel: NS operand stages + 4 raw stages (or the split-K
 // partials, whichever is larger) + barriers; at least 114 KB (one CTA per SM).
-bool gemm_tma_plan(GemmPlan& p) {
+bool gemm_tma_plan(GemmPlan& p, bool bpre) {
   using namespace tw::gemm;
-  const size_t raw = (size_t)A_RAW_BYTES + (size_t)p.BN * BK;
+  const size_t raw = bpre ? 0 : (size_t)p.BN * BK;
   const size_t op = (size_t)A_STAGE_BYTES + (size_t)p.BN * BK * 2;
-  const size_t budget = 200 * 1024 - kRawStages * raw;
-  int ns = (int)(budget / op);
+  const size_t fixed = (size_t)kARing * A_RAW_BYTES + (bpre ? 0 : (size_t)kRawStages * raw);
+  int ns = (int)((200 * 1024 - fixed) / op);
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns > p.kstages_per_split) ns = p.kstages_per_split < 2 ? 2 : p.kstages_per_split;
   if (ns < 2) return false;
   p.nstages = ns;
-  size_t body = (size_t)ns * op + kRawStages * raw;
+  size_t body = (size_t)ns * op + fixed;
   const size_t partial = (size_t)p.BN * BM * 4;
   if (p.ksplit > 1 && body < partial) body = partial;
   p.ctrl_off = (uint32_t)body;
-  p.smem = 1024 + body + 16 * kRawStages + 16 * kMaxStages + 16;
+  p.smem = 1024 + body + kCtrlBytes;
   if (p.smem < 114 * 1024) p.smem = 114 * 1024;
   return p.smem <= 227 * 1024;
 }
 
 }  // namespace
 
+size_t tw_gemm_ws_size(long long M, long long K) { return (size_t)(M * K * 2); }
+
 cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
-                           int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream, int num_sms,
-                           int* unsupported) {
+                           int M, int N, int K, float* y, int32_t* acc_out, void* workspace, cudaStream_t stream,
+                           int num_sms, int* unsupported) {
   using namespace tw::gemm;
   *unsupported = 0;
   if (K % 64 == 0) {
     GemmPlan p;
     CUtensorMap mapA, mapB;
-    if (gemm_plan(M, N, K, num_sms, p) && gemm_tma_plan(p) &&
-        encode_bytes_2d(&mapA, packed, (uint64_t)K / 4, (uint64_t)N, BK / 4, BM) &&
-        encode_bytes_2d(&mapB, x_q, (uint64_t)K, (uint64_t)M, BK, (uint32_t)p.BN)) {
+    const bool bpre = workspace != nullptr;
+    bool ok = gemm_plan(M, N, K, num_sms, p) && gemm_tma_plan(p, bpre) &&
+              encode_bytes_2d(&mapA, packed, (uint64_t)K / 4, (uint64_t)N, BK / 4, BM);
+    if (ok && bpre)
+      ok = encode_2d(&mapB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, workspace, (uint64_t)K, (uint64_t)M, BK,
+                     (uint32_t)p.BN, CU_TENSOR_MAP_SWIZZLE_128B);
+    else if (ok)
+      ok = encode_bytes_2d(&mapB, x_q, (uint64_t)K, (uint64_t)M, BK, (uint32_t)p.BN);
+    if (ok) {
+      if (bpre) {
+        const long long groups = (long long)M * K / 16;
+        widen_acts_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(x_q, groups,
+                                                                                  static_cast<uint4*>(workspace));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+      }
       Args a = {};
       a.packed = packed; a.w_scale = w_scale; a.x_q = x_q; a.s_x = s_x;
       a.M = M; a.N = N; a.K = K; a.BN = p.BN; a.nstages = p.nstages; a.ksplit = p.ksplit;
       a.kstages_per_split = p.kstages_per_split; a.tmem_cols = p.tmem_cols; a.ctrl_off = p.ctrl_off;
       a.y = y; a.acc_out = acc_out;
-      cudaError_t e = cudaFuncSetAttribute(gemm_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)p.smem);
+      auto kern = bpre ? gemm_tma_kernel<true> : gemm_tma_kernel<false>;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
       if (e != cudaSuccess) return e;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)(p.tiles_n * p.ksplit), (unsigned)p.tiles_m);
@@ -783,7 +919,7 @@ cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const in
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      return cudaLaunchKernelEx(&cfg, gemm_tma_kernel, mapA, mapB, a);
+      return cudaLaunchKernelEx(&cfg, kern, mapA, mapB, a);
     }
   }
   GemmPlan p;

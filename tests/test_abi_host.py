@@ -32,7 +32,7 @@ def test_header_declares_entry_points():
     names = _declared_symbols()
     for expected in ["tw_pack_ternary", "tw_quant_act", "tw_rmsnorm_quant_act", "tw_ternary_gemv",
                      "tw_ternary_gemm", "tw_ternary_matmul", "tw_quant_gemv", "tw_status_string",
-                     "tw_pack_workspace_bytes", "tw_device_status"]:
+                     "tw_pack_workspace_bytes", "tw_device_status", "tw_gemm_workspace_bytes"]:
         assert expected in names
 
 
@@ -72,9 +72,11 @@ def test_null_pointers_rejected(tw):
     assert lib.tw_pack_ternary(None, 4, 4, FAKE, FAKE, FAKE, 4096, None) == tw.TW_ERR_NULL
     assert lib.tw_quant_act(FAKE, 1, 16, None, FAKE, None, None) == tw.TW_ERR_NULL
     assert lib.tw_rmsnorm_quant_act(FAKE, None, 1e-6, 1, 16, FAKE, FAKE, None, None) == tw.TW_ERR_NULL
-    for fn in (lib.tw_ternary_gemv, lib.tw_ternary_gemm, lib.tw_ternary_matmul):
-        assert fn(FAKE, FAKE, None, FAKE, None, 1, 4, 16, FAKE, None, None) == tw.TW_ERR_NULL
-        assert fn(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 16, None, None, None) == tw.TW_ERR_NULL
+    assert lib.tw_ternary_gemv(FAKE, FAKE, None, FAKE, None, 1, 4, 16, FAKE, None, None) == tw.TW_ERR_NULL
+    assert lib.tw_ternary_gemv(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 16, None, None, None) == tw.TW_ERR_NULL
+    for fn in (lib.tw_ternary_gemm, lib.tw_ternary_matmul):
+        assert fn(FAKE, FAKE, None, FAKE, None, 1, 4, 16, FAKE, None, None, 0, None) == tw.TW_ERR_NULL
+        assert fn(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 16, None, None, None, 0, None) == tw.TW_ERR_NULL
     assert lib.tw_quant_gemv(None, None, 1e-6, FAKE, FAKE, 1, 4, 64, FAKE, None, None, None, None,
                              None) == tw.TW_ERR_NULL
     assert lib.tw_device_status(None) == tw.TW_ERR_NULL
@@ -84,8 +86,9 @@ def test_null_pointers_rejected(tw):
                                    (-1, 4, 16), (1, 1 << 31, 16)])
 def test_bad_shapes_rejected(tw, M, N, K):
     lib = tw.lib()
-    for fn in (lib.tw_ternary_gemv, lib.tw_ternary_gemm, lib.tw_ternary_matmul):
-        assert fn(FAKE, FAKE, FAKE, FAKE, None, M, N, K, FAKE, None, None) == tw.TW_ERR_SHAPE
+    assert lib.tw_ternary_gemv(FAKE, FAKE, FAKE, FAKE, None, M, N, K, FAKE, None, None) == tw.TW_ERR_SHAPE
+    for fn in (lib.tw_ternary_gemm, lib.tw_ternary_matmul):
+        assert fn(FAKE, FAKE, FAKE, FAKE, None, M, N, K, FAKE, None, None, 0, None) == tw.TW_ERR_SHAPE
 
 
 def test_gemv_rejects_large_m(tw):
@@ -105,7 +108,17 @@ def test_quant_gemv_shape_checks(tw):
 
 def test_gemm_requires_k_multiple_of_16(tw):
     lib = tw.lib()
-    assert lib.tw_ternary_gemm(FAKE, FAKE, FAKE, FAKE, None, 64, 4, 20, FAKE, None, None) == tw.TW_ERR_SHAPE
+    assert lib.tw_ternary_gemm(FAKE, FAKE, FAKE, FAKE, None, 64, 4, 20, FAKE, None, None, 0, None) == tw.TW_ERR_SHAPE
+
+
+def test_gemm_workspace_checks(tw):
+    lib = tw.lib()
+    need = tw.tw_gemm_workspace_bytes(64, 256)
+    assert need == 64 * 256 * 2
+    assert tw.tw_gemm_workspace_bytes(0, 256) == 0 and tw.tw_gemm_workspace_bytes(4, 6) == 0
+    args = (FAKE, FAKE, FAKE, FAKE, None, 64, 4, 256, FAKE, None)
+    assert lib.tw_ternary_gemm(*args, FAKE, need - 1, None) == tw.TW_ERR_WORKSPACE
+    assert lib.tw_ternary_gemm(*args, FAKE + 16, need, None) == tw.TW_ERR_ALIGN
 
 
 def test_pack_checks(tw):
@@ -125,4 +138,5 @@ def test_alignment_checks(tw):
     assert lib.tw_rmsnorm_quant_act(FAKE, FAKE + 4, 1e-6, 1, 16, FAKE, FAKE, None, None) == tw.TW_ERR_ALIGN
     assert lib.tw_ternary_gemv(FAKE, FAKE + 1, FAKE, FAKE, None, 1, 4, 16, FAKE, None, None) == tw.TW_ERR_ALIGN
     assert lib.tw_ternary_gemv(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 16, FAKE + 2, None, None) == tw.TW_ERR_ALIGN
-    assert lib.tw_ternary_gemm(FAKE, FAKE, FAKE + 4, FAKE, None, 64, 4, 16, FAKE, None, None) == tw.TW_ERR_ALIGN
+    assert lib.tw_ternary_gemm(FAKE, FAKE, FAKE + 4, FAKE, None, 64, 4, 16, FAKE, None, None, 0,
+                               None) == tw.TW_ERR_ALIGN

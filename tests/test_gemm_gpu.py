@@ -33,11 +33,17 @@ def host(t):
     return t.cpu().numpy()
 
 
-def run_gemm(tw, packed, gamma, xq, sx, fn="tw_ternary_gemm"):
+def run_gemm(tw, packed, gamma, xq, sx, fn="tw_ternary_gemm", ws=True):
+    """ws=True passes the optional workspace (activations widened once per call, TMA-loaded
+    with hardware swizzle); ws=False makes every CTA widen its own activation tiles."""
     M, N = xq.shape[0], packed.shape[0]
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     acc = torch.full((M, N), -7, dtype=torch.int32, device="cuda")
-    getattr(tw, fn)(dev(packed), dev(np.array([gamma], np.float32)), dev(xq), dev(sx), y, None, acc)
+    work = None
+    if ws:
+        work = torch.full((tw.tw_gemm_workspace_bytes(M, xq.shape[1]) + 256,), 0x5A, dtype=torch.uint8,
+                          device="cuda")
+    getattr(tw, fn)(dev(packed), dev(np.array([gamma], np.float32)), dev(xq), dev(sx), y, None, acc, workspace=work)
     out = host(y), host(acc)
     assert tw.tw_device_status() == 0
     return out
@@ -59,11 +65,12 @@ def case(M, N, K, seed, outliers=True):
     return packed, gamma, xq, sx, y_ref, acc_ref
 
 
+@pytest.mark.parametrize("ws", [True, False])
 @pytest.mark.parametrize("M", [1, 15, 16, 17, 64, 65, 200, 256, 257])
 @pytest.mark.parametrize("N,K", [(128, 64), (7, 80), (200, 2560), (640, 2560), (300, 6912)])
-def test_gemm_parity(tw, M, N, K):
+def test_gemm_parity(tw, M, N, K, ws):
     packed, gamma, xq, sx, y_ref, acc_ref = case(M, N, K, seed=M * 7 + N + K)
-    y, acc = run_gemm(tw, packed, gamma, xq, sx)
+    y, acc = run_gemm(tw, packed, gamma, xq, sx, ws=ws)
     check(y, acc, y_ref, acc_ref)
 
 
@@ -75,8 +82,9 @@ def test_gemm_layer_shapes(tw, M, N, K):
     check(y, acc, y_ref, acc_ref)
 
 
-@pytest.mark.parametrize("K", [16, 4096, 28672, 65520])
-def test_gemm_extreme_accumulators(tw, K):
+@pytest.mark.parametrize("ws", [True, False])
+@pytest.mark.parametrize("K", [16, 4096, 28672, 65472, 65520])
+def test_gemm_extreme_accumulators(tw, K, ws):
     """Tokens chosen as +-127/-128 times a weight row's signs give |acc| = 127..128 * nnz,
     up to 8.4e6 (< 2^24): every partial sum must stay exact in the fp32 accumulation."""
     N, M = 160, 48
@@ -97,13 +105,13 @@ def test_gemm_extreme_accumulators(tw, K):
     sx = np.linspace(0.5, 40.0, M).astype(np.float32)
     y_ref, acc_ref = oracle.ternary_matmul(packed, gamma, xq, sx)
     assert np.abs(acc_ref).max() > 100 * K // 4
-    y, acc = run_gemm(tw, packed, gamma, xq, sx)
+    y, acc = run_gemm(tw, packed, gamma, xq, sx, ws=ws)
     check(y, acc, y_ref, acc_ref)
 
 
 def test_gemm_repeatable(tw):
     packed, gamma, xq, sx, y_ref, acc_ref = case(96, 1000, 2560, seed=5)
-    outs = [run_gemm(tw, packed, gamma, xq, sx) for _ in range(3)]
+    outs = [run_gemm(tw, packed, gamma, xq, sx, ws=w) for w in (True, True, False)]
     for y, acc in outs:
         check(y, acc, y_ref, acc_ref)
         assert (y == outs[0][0]).all()
