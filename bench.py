@@ -47,6 +47,18 @@ FALLBACK_HBM_GBS = 6400.0
 LAYERS = 30
 MODEL = "2B"
 WORKLOAD = "2B-shaped decoder layer, batch 1 (hidden 2560, ffn 6912, 20/5 heads), 30 distinct layers"
+
+# --workload: the default is the decode-layer configuration the metric is quoted on; the
+# others are the batched-decode, 8B and 70B sweeps (each prints its own line).
+# name: (model, layers, M, distinct packed layers generated (the rest are byte copies))
+WORKLOADS = {
+    "2b": ("2B", 30, 1, 30),
+    "2b_m8": ("2B", 30, 8, 30), "2b_m64": ("2B", 30, 64, 30), "2b_m256": ("2B", 30, 256, 30),
+    "8b_m1": ("8B", 32, 1, 4), "8b_m16": ("8B", 32, 16, 4),
+    "70b_m1": ("70B", 80, 1, 1), "70b_m4": ("70B", 80, 4, 1), "70b_m16": ("70B", 80, 16, 1),
+}
+SHAPE_TEXT = {"2B": "hidden 2560, ffn 6912, 20/5 heads", "8B": "hidden 4096, ffn 14336, 32/8 heads",
+              "70B": "hidden 8192, ffn 28672, 64/8 heads"}
 GEMV_SOURCES = ["ternary_weight_quant_b300/csrc/tw_gemv_stream.cu", "ternary_weight_quant_b300/csrc/tw_common.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_dram_traffic.json")
 
@@ -80,9 +92,9 @@ def barrier(world):
 
 
 # ------------------------------------------------------------------ shapes and bytes
-def layer_plan():
+def layer_plan(model=MODEL):
     import seeded_inputs as si
-    s = si.fused_layer_shapes(MODEL)
+    s = si.fused_layer_shapes(model)
     # (name, N, K, prologue) in step order; prologue: "rms" = RMSNorm+quant, "quant" = quant only
     return [("qkv", *s["qkv"], "rms"), ("o", *s["o"], "quant"), ("gateup", *s["gateup"], "rms"),
             ("down", *s["down"], "quant")]
@@ -93,8 +105,13 @@ def gemv_bytes(N, K, M=1):
     return N * K // 4 + M * K + 4 + 4 * M
 
 
-def step_bytes(M=1):
-    return LAYERS * sum(gemv_bytes(N, K, M) for _, N, K, _ in layer_plan())
+def step_bytes(M=1, model=MODEL, layers=LAYERS):
+    return layers * sum(gemv_bytes(N, K, M) for _, N, K, _ in layer_plan(model))
+
+
+def step_ops(M, model=MODEL, layers=LAYERS):
+    """Integer operations of one step (2 per weight and token)."""
+    return layers * sum(2 * M * N * K for _, N, K, _ in layer_plan(model))
 
 
 def measured_peaks():
@@ -104,6 +121,16 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s measured on this machine (the tensor path computes in bf16 operands)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured bf16 burst"
+    return 1800.0, "fallback"
 
 
 def source_hash(paths):
@@ -252,31 +279,42 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU workload
 class DecodeStack:
-    """30 layers of packed weights, activations and outputs resident on the GPU.
+    """Layers of packed weights, activations and outputs resident on the GPU.
 
     All activation inputs of a step live in one flat device buffer and all outputs in
-    another, so the end-to-end measurement moves each direction in one copy."""
+    another, so the end-to-end measurement moves each direction in one copy.  The first
+    `distinct` layers are drawn and packed from their own seeds; further layers are
+    byte copies of them in their own memory (the stream is what is measured)."""
 
-    def __init__(self, tw, layers: int, M: int = 1, seed: int = 1234):
+    def __init__(self, tw, layers: int, M: int = 1, seed: int = 1234, model: str = MODEL, distinct=None):
         import torch
         import seeded_inputs as si
-        self.tw, self.M, self.layers = tw, M, layers
-        self.plan = layer_plan()
+        self.tw, self.M, self.layers, self.model = tw, M, layers, model
+        self.plan = layer_plan(model)
+        distinct = layers if distinct is None else distinct
         n_in = layers * sum(M * K for _, N, K, _ in self.plan)
         n_out = layers * sum(M * N for _, N, K, _ in self.plan)
         self.x_all = torch.empty(n_in, dtype=torch.float32, device="cuda")
         self.y_all = torch.empty(n_out, dtype=torch.float32, device="cuda")
         self.L = []
-        ws = torch.empty(tw.tw_pack_workspace_bytes(13824, 2560), dtype=torch.uint8, device="cuda")
+        maxNK = max(N * K for _, N, K, _ in self.plan)
+        ws = torch.empty(tw.tw_pack_workspace_bytes(1, 4), dtype=torch.uint8, device="cuda")
+        maxMK = max(M * K for _, N, K, _ in self.plan)
+        self.gemm_ws = tw.gemm_workspace(M, max(K for _, N, K, _ in self.plan)) if M > 4 else None
         oi = oo = 0
         for l in range(layers):
             d = {}
             for i, (name, N, K, pro) in enumerate(self.plan):
-                W = si.device_normal((N, K), seed=seed + 1000 * l + i)
                 packed = torch.empty((N, K // 4), dtype=torch.uint8, device="cuda")
                 gamma = torch.empty(1, dtype=torch.float32, device="cuda")
-                tw.tw_pack_ternary(W, packed, gamma, ws)
-                del W
+                if l < distinct:
+                    W = si.device_normal((N, K), seed=seed + 1000 * l + i)
+                    tw.tw_pack_ternary(W, packed, gamma, ws)
+                    del W
+                else:
+                    src = self.L[l % distinct][name]
+                    packed.copy_(src["packed"])
+                    gamma.copy_(src["gamma"])
                 x = self.x_all[oi:oi + M * K].view(M, K)
                 oi += M * K
                 x.copy_(si.device_normal((M, K), seed=seed + 1000 * l + 100 + i))
@@ -288,10 +326,34 @@ class DecodeStack:
                                s_x=torch.empty(M, dtype=torch.float32, device="cuda"),
                                x_sum=torch.empty(M, dtype=torch.int32, device="cuda"))
             self.L.append(d)
+        del maxNK, maxMK
+        self._fused_ok = {}
         torch.cuda.synchronize()
 
     def launches_per_step(self, fused=True):
-        return self.layers * len(self.plan) * (1 if fused else 2)
+        """Kernel launches of one step: 1 per GEMV when fused; otherwise the quantisation
+        plus the GEMV (M <= 16) or plus the activation widening and the GEMM (M > 16)."""
+        n = 0
+        for name, N, K, pro in self.plan:
+            if fused and self._fused_ok.get((N, K), True):
+                n += 1
+            else:
+                n += 2 if self.M <= 16 else 3
+        return self.layers * n
+
+    def fused_ok(self, e):
+        """Whether the fused quantisation + GEMV kernel takes this shape (decided once)."""
+        key = (e["N"], e["K"])
+        if key not in self._fused_ok:
+            import seeded_inputs as si
+            try:
+                self.tw.tw_quant_gemv(e["x"], e["packed"], e["gamma"], e["y"], g=e["g"], eps=si.RMS_EPS)
+                self._fused_ok[key] = True
+            except self.tw.TWError as err:
+                if err.status != self.tw.TW_ERR_UNSUPPORTED:
+                    raise
+                self._fused_ok[key] = False
+        return self._fused_ok[key]
 
     def enqueue(self, events=None, fused=True):
         """Enqueue one step on the current stream (optionally with events around each GEMV).
@@ -303,7 +365,8 @@ class DecodeStack:
         for d in self.L:
             for name, N, K, pro in self.plan:
                 e = d[name]
-                if not fused:
+                fz = fused and self.fused_ok(e)
+                if not fz:
                     if pro == "rms":
                         tw.tw_rmsnorm_quant_act(e["x"], e["g"], si.RMS_EPS, e["x_q"], e["s_x"], e["x_sum"])
                     else:
@@ -311,10 +374,11 @@ class DecodeStack:
                 if events is not None:
                     a, b = events_new(), events_new()
                     a.record()
-                if fused:
+                if fz:
                     tw.tw_quant_gemv(e["x"], e["packed"], e["gamma"], e["y"], g=e["g"], eps=si.RMS_EPS)
                 else:
-                    tw.tw_ternary_gemv(e["packed"], e["gamma"], e["x_q"], e["s_x"], e["y"], e["x_sum"])
+                    tw.tw_ternary_matmul(e["packed"], e["gamma"], e["x_q"], e["s_x"], e["y"], e["x_sum"],
+                                         workspace=self.gemm_ws)
                 if events is not None:
                     b.record()
                     events.append((name, a, b))
@@ -354,9 +418,12 @@ def run_ours(args):
     torch.cuda.set_device(local)
     import ternary_weight_quant_b300 as tw
 
-    fused = not args.separate
-    stack = DecodeStack(tw, LAYERS, M=1)
-    bytes_per_step = step_bytes(1)
+    model, layers, M, distinct = WORKLOADS[args.workload]
+    fused = (not args.separate) and M <= 4
+    stack = DecodeStack(tw, layers, M=M, model=model, distinct=distinct)
+    plan = layer_plan(model)
+    bytes_per_step = step_bytes(M, model, layers)
+    ops_per_step = step_ops(M, model, layers)
     graph = capture(stack, fused)
     for _ in range(args.warmup):
         graph.replay()
@@ -379,9 +446,9 @@ def run_ours(args):
     elapsed_max, total_bytes = combine_over_ranks(elapsed, bytes_per_step * args.steps, world)
     value = total_bytes / elapsed_max / 1e9
     ms_per_step = elapsed_max / args.steps * 1e3
-    us_per_layer = ms_per_step * 1e3 / LAYERS
+    us_per_layer = ms_per_step * 1e3 / layers
 
-    # ---- roofline of the GEMV kernel: events around each GEMV launch of extra steps
+    # ---- roofline of the product kernel: events around each product launch of extra steps
     per_launch = {}
     for rep in range(3):
         evs = []
@@ -392,14 +459,20 @@ def run_ours(args):
             continue
         for name, a, b in evs:
             per_launch.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
-    gemv_time = sum(sum(v) for v in per_launch.values())
-    gemv_launches = sum(len(v) for v in per_launch.values())
-    shapes = {name: (N, K) for name, N, K, _ in layer_plan()}
-    gemv_bytes_total = sum(gemv_bytes(*shapes[n]) * len(v) for n, v in per_launch.items())
-    achieved = gemv_bytes_total / gemv_time / 1e9
-    peak, peak_kind = measured_peaks()
-    per_shape = {n: {"bytes": gemv_bytes(*shapes[n]), "us_median": statistics.median(v) * 1e6,
-                     "GB/s": gemv_bytes(*shapes[n]) / statistics.median(v) / 1e9}
+    prod_time = sum(sum(v) for v in per_launch.values())
+    prod_launches = sum(len(v) for v in per_launch.values())
+    shapes = {name: (N, K) for name, N, K, _ in plan}
+    peak_hbm, peak_kind = measured_peaks()
+    if M <= 16:
+        algo = sum(gemv_bytes(*shapes[n], M) * len(v) for n, v in per_launch.items())
+        achieved, peak, unit, bound = algo / prod_time / 1e9, peak_hbm, "GB/s", "hbm"
+    else:
+        algo = sum(2 * M * shapes[n][0] * shapes[n][1] * len(v) for n, v in per_launch.items())
+        peak, pk = measured_tensor_peak()
+        achieved, unit, bound, peak_kind = algo / prod_time / 1e12, "TFLOP/s", "tensor", pk
+    per_shape = {n: {"bytes": gemv_bytes(*shapes[n], M), "us_median": statistics.median(v) * 1e6,
+                     "GB/s": gemv_bytes(*shapes[n], M) / statistics.median(v) / 1e9,
+                     "TFLOP/s": 2 * M * shapes[n][0] * shapes[n][1] / statistics.median(v) / 1e12}
                  for n, v in per_launch.items()}
 
     # ---- e2e: inputs from pinned host, outputs back to pinned host, per step (one copy each way)
@@ -427,37 +500,49 @@ def run_ours(args):
     e2e_el, e2e_bytes = combine_over_ranks(e0.elapsed_time(e1) / 1e3, bytes_per_step * e2e_steps, world)
     e2e_value = e2e_bytes / e2e_el / 1e9
 
-    # ---- CPU baseline: the oracle on the host, bounded sample (rank 0, N = 1 only)
+    # ---- CPU baseline: the oracle on the host, bounded sample (rank 0, N = 1, default workload)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        layers = host_oracle_layers(1)
-        b, el, n = oracle_layer_sample(layers, args.cpu_seconds, 3 * args.cpu_seconds)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "2b":
+        olayers = host_oracle_layers(1)
+        b, el, n = oracle_layer_sample(olayers, args.cpu_seconds, 3 * args.cpu_seconds)
         cpu = {"value": b / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} run(s) of one 2B-shaped layer (RMSNorm/quant + 4 GEMVs, M=1), "
                          f"single thread, {el:.1f} s"}
 
     if rank == 0:
-        kern = "tw::gemv_stream_kernel<1,8,fused>" if fused else "tw::gemv_stream_kernel<1,8>"
+        if fused:
+            kern = "tw::gemv_stream_kernel (quantisation fused)"
+        elif M <= 16:
+            kern = "tw::gemv_stream_kernel / gemv_dp4a_kernel"
+        else:
+            kern = "tw::gemm::gemm_tok_kernel / gemm_tma_kernel (tcgen05)"
+        launches = stack.launches_per_step(fused)
+        workload = (WORKLOAD if args.workload == "2b" else
+                    f"{model}-shaped decoder layer, batch {M} ({SHAPE_TEXT[model]}), {layers} layers "
+                    f"({distinct} drawn, the rest byte copies in their own memory)")
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": 1, "layers": LAYERS, "hidden": 2560, "ffn": 6912,
-                       "bytes_per_step": bytes_per_step, "launches_per_step": stack.launches_per_step(fused),
+            "config": {"workload": workload, "M": M, "layers": layers,
+                       "bytes_per_step": bytes_per_step, "int_ops_per_step": ops_per_step,
+                       "launches_per_step": launches,
                        "quantisation": "fused into the GEMV launch" if fused else "separate kernels",
                        "graph": "one CUDA graph per step",
-                       "l2": "working set 521 MB > 4x the 126 MB L2; no flush needed",
+                       "l2": f"working set {bytes_per_step / 1e6:.0f} MB of packed weights, > 4x the 126 MB L2; "
+                             "no flush needed",
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": us_per_layer,
+            "TFLOP/s": ops_per_step * args.steps * world / elapsed_max / 1e12,
             "pct_of_nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
-            "pct_of_measured_copy": 100.0 * value / world / peak,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": recorded_traffic(),
+            "pct_of_measured_copy": 100.0 * value / world / peak_hbm,
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                         "frac": achieved / peak, "traffic": recorded_traffic() if fused else None,
                          "kernel": kern, "peak_source": peak_kind,
-                         "launches_timed": gemv_launches, "per_shape": per_shape},
+                         "launches_timed": prod_launches, "per_shape": per_shape},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": stack.launches_per_step(fused) * args.steps,
+            "gpu_launches": launches * args.steps,
             "clocks": clocks.summary(),
             "wall_s_timed": t_wall,
         }
@@ -548,6 +633,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--separate", action="store_true", help="quantisation as separate kernels")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="2b",
+                    help="2b (the default decode-layer configuration), 2b_m8/m64/m256, 8b_m1/m16, 70b_m1/m4/m16")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-case", default=None,

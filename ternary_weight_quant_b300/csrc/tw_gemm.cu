@@ -272,14 +272,14 @@ __device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* pa
             __cluster_map_shared_rank((void*)(part + (size_t)t0 * BM), (unsigned)(rk < a.ksplit ? rk : 0)));
       const int nvec = (t1 - t0) * BM / 4;
       for (int e = tid; e < nvec; e += NTHR) {
+        float4 v[kMaxCluster];  // every rank's partials in flight together
+#pragma unroll
+        for (int rk = 0; rk < kMaxCluster; ++rk) v[rk] = rk < a.ksplit ? src[rk][e] : make_float4(0.f, 0.f, 0.f, 0.f);
         int4 acc = make_int4(0, 0, 0, 0);
 #pragma unroll
         for (int rk = 0; rk < kMaxCluster; ++rk) {
-          if (rk < a.ksplit) {
-            const float4 v = src[rk][e];
-            acc.x += __float2int_rn(v.x); acc.y += __float2int_rn(v.y);
-            acc.z += __float2int_rn(v.z); acc.w += __float2int_rn(v.w);
-          }
+          acc.x += __float2int_rn(v[rk].x); acc.y += __float2int_rn(v[rk].y);
+          acc.z += __float2int_rn(v[rk].z); acc.w += __float2int_rn(v[rk].w);
         }
         const int j = t0 + (4 * e) / BM, rr = (4 * e) % BM;
         const int m = m0 + j;
@@ -753,6 +753,282 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 }
 
 
+// ----------------------------------------------------------------------------
+// Tokens-on-M variant (1 <= M <= 128, K % 64 == 0, activations pre-widened into the
+// workspace).  One tcgen05.mma costs the same time whatever its N, so the
+// instruction count is what matters: with the tokens (padded to 128) as the MMA's
+// M side and 256 weight rows as its N side, a weight tile needs half the
+// instructions of a 128-row tile.  The accumulators are [128 tokens][256 rows]
+// in tensor memory: each thread of the epilogue owns one token and writes runs of
+// 32 consecutive outputs.
+constexpr int TBN = 256;                       // weight rows per CTA (MMA N)
+constexpr int TB_STAGE = TBN * BK * 2;         // 32 KB of widened weights per stage
+constexpr int TA_STAGE = 128 * BK * 2;         // 16 KB of activations per stage
+constexpr int TW_RAW = TBN * (BK / 4);         // 4 KB of packed codes per stage
+constexpr int kTokARing = 8;
+
+// Epilogue of the tokens-on-M kernel.  Warp w reads tensor-memory lanes 32 (w % 4)
+// .. +31 (its tokens) and the weight-row half w / 4.  `part` (split-K) holds
+// [256 rows][128 tokens] partial sums.
+__device__ __forceinline__ void tok_epilogue(const Args& a, uint32_t tmem, float* part, volatile int* abort_flag,
+                                             int any_fail, int nk, int n0, uint32_t crank, const float* scale) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int m = quarter * 32 + lane;  // token of this thread
+  const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+  const float gam = __ldg(a.w_scale);
+  const bool vec = (a.N & 3) == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(a.acc_out) & 15) == 0;  // 16-byte stores allowed
+  int cluster_fail = any_fail;
+  auto store_run = [&](int nbase, const int* acc, int cnt) {  // outputs nbase .. nbase+cnt-1 of token m
+    if (m >= a.M) return;
+    const float sm = scale[m], c = scale[128 + m];
+    float* yrow = a.y + (size_t)m * a.N;
+    int32_t* arow = a.acc_out ? a.acc_out + (size_t)m * a.N : nullptr;
+    for (int t = 0; t < cnt; t += 4) {
+      const int n = nbase + t;
+      if (vec && n + 4 <= a.N) {
+        const float4 v = make_float4(dequant(acc[t], c, gam, sm), dequant(acc[t + 1], c, gam, sm),
+                                     dequant(acc[t + 2], c, gam, sm), dequant(acc[t + 3], c, gam, sm));
+        *reinterpret_cast<float4*>(yrow + n) = v;
+        if (arow) *reinterpret_cast<int4*>(arow + n) = make_int4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
+      } else {
+        for (int q = 0; q < 4; ++q) {
+          if (n + q < a.N) {
+            yrow[n + q] = dequant(acc[t + q], c, gam, sm);
+            if (arow) arow[n + q] = acc[t + q];
+          }
+        }
+      }
+    }
+  };
+  const bool warp_live = quarter * 32 < a.M;  // some token of this warp is real (warp-uniform)
+  if (a.ksplit > 1) {
+    if (warp < 8 && warp_live && !any_fail) {
+      for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
+        uint32_t v[32];
+        if (nk > 0) {
+          tmem_ld32(taddr + (uint32_t)c0, v);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = 0u;
+        }
+#pragma unroll
+        for (int t = 0; t < 32; ++t) part[(size_t)(c0 + t) * 128 + m] = __uint_as_float(v[t]);
+      }
+    }
+    if (tid == 0) *abort_flag = any_fail;
+    cluster_sync();
+    for (int rk = 0; rk < a.ksplit; ++rk)
+      cluster_fail |= *static_cast<volatile int*>(__cluster_map_shared_rank((void*)abort_flag, (unsigned)rk));
+    if (!cluster_fail) {
+      // CTA crank finishes weight rows [r0, r0 + per) of the tile.  Work item = (row,
+      // group of 4 real tokens): one float4 from every rank's partials, all loads in
+      // flight together, then up to 4 scalar stores.
+      const int per = TBN / a.ksplit;
+      const int r0 = (int)crank * per;
+      const int tg = (a.M + 3) >> 2;
+      const float4* src[kMaxCluster];
+#pragma unroll
+      for (int rk = 0; rk < kMaxCluster; ++rk)
+        src[rk] = static_cast<const float4*>(__cluster_map_shared_rank((void*)part, (unsigned)(rk < a.ksplit ? rk : 0)));
+      for (int it = tid; it < per * tg; it += kTmaThreads) {
+        const int rr = r0 + it / tg, g = it % tg;
+        float4 v[kMaxCluster];
+#pragma unroll
+        for (int rk = 0; rk < kMaxCluster; ++rk)
+          v[rk] = rk < a.ksplit ? src[rk][(size_t)rr * 32 + g] : make_float4(0.f, 0.f, 0.f, 0.f);
+        int acc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int rk = 0; rk < kMaxCluster; ++rk) {
+          acc[0] += __float2int_rn(v[rk].x); acc[1] += __float2int_rn(v[rk].y);
+          acc[2] += __float2int_rn(v[rk].z); acc[3] += __float2int_rn(v[rk].w);
+        }
+        const int n = n0 + rr;
+        if (n < a.N) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int mm = 4 * g + q;
+            if (mm < a.M) {
+              a.y[(size_t)mm * a.N + n] = dequant(acc[q], scale[128 + mm], gam, scale[mm]);
+              if (a.acc_out) a.acc_out[(size_t)mm * a.N + n] = acc[q];
+            }
+          }
+        }
+      }
+    }
+    cluster_sync();  // no CTA leaves while others still read its shared memory
+  } else if (warp < 8 && warp_live && !any_fail) {
+    for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(taddr + (uint32_t)c0, v);
+      int acc[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) acc[t] = __float2int_rn(__uint_as_float(v[t]));
+      store_run(n0 + c0, acc, 32);
+    }
+  }
+  if (tid == 0 && cluster_fail) atomicExch(&g_gemm_status, (int)TW_ERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    gemm_tok_kernel(const __grid_constant__ CUtensorMap mapX, Args a) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw0 = smem_u32(smem_raw);
+  const uint32_t base = (raw0 + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw0);
+  const int NS = a.nstages;
+  const uint32_t op_bytes = TA_STAGE + TB_STAGE;  // 48 KB: activations, then weights
+  const uint32_t op0 = base;
+  const uint32_t wraw = base + (uint32_t)NS * op_bytes;  // [kTokARing][256 rows][16 B]
+  unsigned char* ctrl = gbase + a.ctrl_off;
+  const uint32_t op_full = smem_u32(ctrl);  // [kMaxStages]
+  const uint32_t op_empty = op_full + 8 * kMaxStages;
+  const uint32_t bar_done = op_empty + 8 * kMaxStages;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctrl + 16 * kMaxStages + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 16 * kMaxStages + 12);
+  float* scale = reinterpret_cast<float*>(ctrl + kScaleOff);  // [128] s_x, [128] dequantisation scales
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = a.ksplit > 1 ? cluster_ctarank() : 0u;
+  const int n0 = blockIdx.x / a.ksplit * TBN;
+  const int kst0 = (int)crank * a.kstages_per_split;
+  const int nk = max(0, min(a.kstages_per_split, a.K / BK - kst0));
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(op_full + 8 * s, kTmaConv / 32 + 1);
+      mbar_init(op_empty + 8 * s, 1);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32((const void*)tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ activation tiles
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapX)) : "memory");
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % NS;
+        if (i >= NS && !mbar_wait(op_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(op_full + 8 * s, (uint32_t)TA_STAGE);
+        tma_load_2d(op0 + (uint32_t)s * op_bytes, &mapX, (kst0 + i) * BK, 0, op_full + 8 * s);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(op_full + 8 * (i % NS), (uint32_t)((i / NS) & 1));
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issue (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TBN >> 3) << 17) | ((128u >> 4) << 24);
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % NS;
+        if (!mbar_wait(op_full + 8 * s, (uint32_t)((i / NS) & 1), abort_flag) || *abort_flag) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t As = op0 + (uint32_t)s * op_bytes, Bs = As + TA_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16(tmem, sw128_desc(As + 32 * kk), sw128_desc(Bs + 32 * kk), idesc, (i | kk) ? 1u : 0u);
+        mma_commit(op_empty + 8 * s);
+      }
+      mma_commit(bar_done);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ weight converters (warps 0-7)
+    for (int j = tid; j < 128; j += kTmaConv) {
+      const float sm = j < a.M ? __ldg(a.s_x + j) : 0.0f;
+      scale[j] = sm;
+      scale[128 + j] = dequant_scale(__ldg(a.w_scale), sm);
+    }
+    const int r = tid;  // weight row of the tile owned by this thread
+    const bool rowv = n0 + r < a.N;
+    const uint8_t* gW = a.packed + (size_t)(rowv ? n0 + r : 0) * (a.K / 4);
+    const uint32_t rslot = wraw + (uint32_t)(r * 16);
+    auto fetch = [&](int i) {
+      if (i < nk && rowv) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(rslot + (uint32_t)(i % kTokARing) * TW_RAW),
+                     "l"(gW + (size_t)(kst0 + i) * (BK / 4))
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+#pragma unroll
+    for (int i = 0; i < kTokARing; ++i) fetch(i);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % NS;
+      asm volatile("cp.async.wait_group %0;" ::"n"(kTokARing - 1) : "memory");
+      int okw = 1;
+      if (lane == 0) okw = i < NS || mbar_wait(op_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag);
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      __syncwarp();
+      if (!okw) {
+        ok = false;
+        *abort_flag = 1;
+        break;
+      }
+      uint4 w;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                   : "r"(rslot + (uint32_t)(i % kTokARing) * TW_RAW));
+      if (!rowv) w = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+      fetch(i + kTokARing);
+      const uint32_t Bs = op0 + (uint32_t)s * op_bytes + TA_STAGE;
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 lo, hi;
+        widen_codes(wv[q], lo, hi);
+        st_shared_v4(Bs + sw128_off(r, 2 * q), lo);
+        st_shared_v4(Bs + sw128_off(r, 2 * q + 1), hi);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(op_full + 8 * s);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+
+  const bool done_ok = mbar_wait(bar_done, 0);
+  tc_fence_after();
+  __syncthreads();
+  const bool failed = !done_ok || *abort_flag != 0 || !ok;
+  const int any_fail = __syncthreads_or(failed ? 1 : 0);
+  tok_epilogue(a, tmem, reinterpret_cast<float*>(gbase), abort_flag, any_fail, nk, n0, crank, scale);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
+
 // x_q [M][K] int8 -> bf16 [M][K], each 16-element group in the MMA K order
 // 0,4,1,5,2,6,3,7,8,12,9,13,10,14,11,15 (the order widen_codes gives the weights).
 __global__ void __launch_bounds__(256) widen_acts_kernel(const int8_t* __restrict__ x_q, long long groups,
@@ -875,11 +1151,77 @@ bool gemm_tma_plan(GemmPlan& p, bool bpre) {
 
 size_t tw_gemm_ws_size(long long M, long long K) { return (size_t)(M * K * 2); }
 
+namespace {
+
+// Tokens-on-M plan: ceil(N / 256) weight tiles, K split over a cluster so that the
+// grid comes close to one CTA per SM without slicing K below 8 stages.
+bool gemm_tok_plan(int M, int N, int K, int num_sms, GemmPlan& p) {
+  using namespace tw::gemm;
+  if (M > 128 || K % 64 != 0) return false;
+  p.BN = 128;
+  p.tiles_n = (N + TBN - 1) / TBN;
+  p.tiles_m = 1;
+  const int nkst = K / BK;
+  p.ksplit = 1;
+  while (p.ksplit < kMaxCluster && (long long)p.tiles_n * (p.ksplit * 2) <= num_sms && nkst / (p.ksplit * 2) >= 8)
+    p.ksplit *= 2;
+  p.kstages_per_split = (nkst + p.ksplit - 1) / p.ksplit;
+  const size_t op = (size_t)TA_STAGE + TB_STAGE;
+  const size_t fixed = (size_t)kTokARing * TW_RAW;
+  int ns = (int)((200 * 1024 - fixed) / op);
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns > p.kstages_per_split) ns = p.kstages_per_split < 2 ? 2 : p.kstages_per_split;
+  if (ns < 2) return false;
+  p.nstages = ns;
+  size_t body = (size_t)ns * op + fixed;
+  const size_t partial = (size_t)TBN * 128 * 4;
+  if (p.ksplit > 1 && body < partial) body = partial;
+  p.ctrl_off = (uint32_t)body;
+  p.smem = 1024 + body + kCtrlBytes;
+  if (p.smem < 114 * 1024) p.smem = 114 * 1024;
+  p.tmem_cols = 256;
+  return p.smem <= 227 * 1024;
+}
+
+}  // namespace
+
 cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
                            int M, int N, int K, float* y, int32_t* acc_out, void* workspace, cudaStream_t stream,
                            int num_sms, int* unsupported) {
   using namespace tw::gemm;
   *unsupported = 0;
+  GemmPlan tp;
+  if (workspace != nullptr && gemm_tok_plan(M, N, K, num_sms, tp)) {
+    CUtensorMap mapX;
+    if (encode_2d(&mapX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, workspace, (uint64_t)K, (uint64_t)M, BK, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B)) {
+      const long long groups = (long long)M * K / 16;
+      widen_acts_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(x_q, groups,
+                                                                                static_cast<uint4*>(workspace));
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      Args a = {};
+      a.packed = packed; a.w_scale = w_scale; a.x_q = x_q; a.s_x = s_x;
+      a.M = M; a.N = N; a.K = K; a.BN = tp.BN; a.nstages = tp.nstages; a.ksplit = tp.ksplit;
+      a.kstages_per_split = tp.kstages_per_split; a.tmem_cols = tp.tmem_cols; a.ctrl_off = tp.ctrl_off;
+      a.y = y; a.acc_out = acc_out;
+      e = cudaFuncSetAttribute(gemm_tok_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tp.smem);
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(tp.tiles_n * tp.ksplit), 1);
+      cfg.blockDim = dim3(kTmaThreads);
+      cfg.dynamicSmemBytes = tp.smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)tp.ksplit;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, gemm_tok_kernel, mapX, a);
+    }
+  }
   if (K % 64 == 0) {
     GemmPlan p;
     CUtensorMap mapA, mapB;

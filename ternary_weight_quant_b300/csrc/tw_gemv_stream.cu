@@ -466,7 +466,15 @@ bool make_plan(int M, int N, int K, int num_sms, Plan& p, bool fused) {
     }
   }
   if (p.S == 0) return false;
-  p.grid = N < num_sms ? N : num_sms;
+  // One CTA per SM leaves the second slot to the next launch (programmatic dependent
+  // launch).  Matrices whose rows per warp group exceed what one batch of registers
+  // holds stream for long enough that two CTAs per SM (twice the loads in flight) pay
+  // off more than the overlap with the next launch.
+  const int G = tw::kWarps / p.S;
+  const int pre = MT == 1 ? (p.jmax <= 5 ? 8 : 6) : MT == 2 ? (p.jmax <= 2 ? 8 : 6) : (p.jmax <= 1 ? 8 : 4);
+  const bool long_stream = (long long)N > (long long)num_sms * G * pre;
+  const int ctas = long_stream ? 2 * num_sms : num_sms;
+  p.grid = N < ctas ? N : ctas;
   p.rows_base = N / p.grid;
   p.rows_rem = N % p.grid;
   const int max_rows = p.rows_base + (p.rows_rem ? 1 : 0);

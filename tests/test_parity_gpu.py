@@ -384,6 +384,23 @@ def test_quant_gemv_chain_pdl(tw):
         assert_y_close(host(bufs[i + 1]), ref[i + 1])
 
 
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_long_stream_two_ctas_per_sm(tw, M):
+    """A matrix with more rows than one register batch of every warp (the kernel then runs
+    two CTAs per SM and loads later batches inside the loop): full comparison."""
+    N, K = 20000, 2560
+    W, x = si.gemv_case(M, N, K, seed=123 + M)
+    p_ref, g_ref = oracle.pack_ternary(W)
+    q_ref, s_ref, sum_ref = oracle.quant_act(x)
+    y_ref, acc_ref = oracle.ternary_matmul(p_ref, g_ref, q_ref, s_ref)
+    y, acc = run_product(tw, "tw_ternary_gemv", p_ref, g_ref, q_ref, s_ref)
+    assert (acc == acc_ref).all()
+    assert_y_close(y, y_ref)
+    yf, accf, xq, _, _, _ = fused_run(tw, x, p_ref, g_ref, None)
+    assert (xq == q_ref).all() and (accf == acc_ref).all()
+    assert_y_close(yf, y_ref)
+
+
 # ----------------------------------------------------------------------------- full decode layer (2B)
 def test_2b_layer_full_parity(tw):
     """Every GEMV of a 2B-shaped decoder layer at M = 1, fully compared (fused q|k|v and gate|up)."""
