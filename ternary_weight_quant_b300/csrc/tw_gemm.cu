@@ -759,17 +759,28 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // instruction count is what matters: with the tokens (padded to 128) as the MMA's
 // M side and 256 weight rows as its N side, a weight tile needs half the
 // instructions of a 128-row tile.  The accumulators are [128 tokens][256 rows]
-// in tensor memory: each thread of the epilogue owns one token and writes runs of
-// 32 consecutive outputs.
+// in tensor memory: each thread of the epilogue owns one token.
+// Pipeline: the activation tiles (TMA, 16 KB) have a ring of their own, deep enough
+// (kTokNA stages) to hide the copy latency behind the MMAs; the widened weight tiles
+// (32 KB) need only kTokNB stages, since their packed codes are fetched kTokARing
+// stages ahead with cp.async.  Launched with programmatic dependent launch: the
+// weight fetches start before the widening kernel in front of it has finished.
 constexpr int TBN = 256;                       // weight rows per CTA (MMA N)
 constexpr int TB_STAGE = TBN * BK * 2;         // 32 KB of widened weights per stage
 constexpr int TA_STAGE = 128 * BK * 2;         // 16 KB of activations per stage
 constexpr int TW_RAW = TBN * (BK / 4);         // 4 KB of packed codes per stage
-constexpr int kTokARing = 8;
+constexpr int kTokNA = 6, kTokNB = 3, kTokARing = 4;
+constexpr int kPartStride = TBN + 4;           // floats per token row of the split-K partials
+constexpr int kTokThreads = 320;               // warps 0-7 convert + epilogue, 8: TMA, 9: MMA
+
+__device__ __forceinline__ void pdl_wait_all() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Epilogue of the tokens-on-M kernel.  Warp w reads tensor-memory lanes 32 (w % 4)
-// .. +31 (its tokens) and the weight-row half w / 4.  `part` (split-K) holds
-// [256 rows][128 tokens] partial sums.
+// .. +31 (its tokens) and the weight-row half w / 4.  With a K split the partial
+// sums go to this CTA's shared memory as [token][kPartStride] and CTA crank of the
+// cluster finishes rows [crank * 256/ksplit, ...) for every real token, reading
+// four consecutive rows at a time from every rank and storing them as one float4.
 __device__ __forceinline__ void tok_epilogue(const Args& a, uint32_t tmem, float* part, volatile int* abort_flag,
                                              int any_fail, int nk, int n0, uint32_t crank, const float* scale) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -779,30 +790,26 @@ __device__ __forceinline__ void tok_epilogue(const Args& a, uint32_t tmem, float
   const float gam = __ldg(a.w_scale);
   const bool vec = (a.N & 3) == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(a.acc_out) & 15) == 0;  // 16-byte stores allowed
+  const bool warp_live = quarter * 32 < a.M;  // some token of this warp is real (warp-uniform)
   int cluster_fail = any_fail;
-  auto store_run = [&](int nbase, const int* acc, int cnt) {  // outputs nbase .. nbase+cnt-1 of token m
-    if (m >= a.M) return;
-    const float sm = scale[m], c = scale[128 + m];
-    float* yrow = a.y + (size_t)m * a.N;
-    int32_t* arow = a.acc_out ? a.acc_out + (size_t)m * a.N : nullptr;
-    for (int t = 0; t < cnt; t += 4) {
-      const int n = nbase + t;
-      if (vec && n + 4 <= a.N) {
-        const float4 v = make_float4(dequant(acc[t], c, gam, sm), dequant(acc[t + 1], c, gam, sm),
-                                     dequant(acc[t + 2], c, gam, sm), dequant(acc[t + 3], c, gam, sm));
-        *reinterpret_cast<float4*>(yrow + n) = v;
-        if (arow) *reinterpret_cast<int4*>(arow + n) = make_int4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
-      } else {
-        for (int q = 0; q < 4; ++q) {
-          if (n + q < a.N) {
-            yrow[n + q] = dequant(acc[t + q], c, gam, sm);
-            if (arow) arow[n + q] = acc[t + q];
-          }
+  // outputs n .. n+3 of token mm
+  auto store4 = [&](int mm, int n, int a0, int a1, int a2, int a3) {
+    const float sm = scale[mm], c = scale[128 + mm];
+    float* yrow = a.y + (size_t)mm * a.N;
+    if (vec && n + 4 <= a.N) {
+      *reinterpret_cast<float4*>(yrow + n) =
+          make_float4(dequant(a0, c, gam, sm), dequant(a1, c, gam, sm), dequant(a2, c, gam, sm), dequant(a3, c, gam, sm));
+      if (a.acc_out) *reinterpret_cast<int4*>(a.acc_out + (size_t)mm * a.N + n) = make_int4(a0, a1, a2, a3);
+    } else {
+      const int av[4] = {a0, a1, a2, a3};
+      for (int q = 0; q < 4; ++q) {
+        if (n + q < a.N) {
+          yrow[n + q] = dequant(av[q], c, gam, sm);
+          if (a.acc_out) a.acc_out[(size_t)mm * a.N + n + q] = av[q];
         }
       }
     }
   };
-  const bool warp_live = quarter * 32 < a.M;  // some token of this warp is real (warp-uniform)
   if (a.ksplit > 1) {
     if (warp < 8 && warp_live && !any_fail) {
       for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
@@ -813,8 +820,11 @@ __device__ __forceinline__ void tok_epilogue(const Args& a, uint32_t tmem, float
 #pragma unroll
           for (int t = 0; t < 32; ++t) v[t] = 0u;
         }
+        float4* dst = reinterpret_cast<float4*>(part + (size_t)m * kPartStride + c0);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) part[(size_t)(c0 + t) * 128 + m] = __uint_as_float(v[t]);
+        for (int t = 0; t < 8; ++t)
+          dst[t] = make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]), __uint_as_float(v[4 * t + 2]),
+                               __uint_as_float(v[4 * t + 3]));
       }
     }
     if (tid == 0) *abort_flag = any_fail;
@@ -822,39 +832,26 @@ __device__ __forceinline__ void tok_epilogue(const Args& a, uint32_t tmem, float
     for (int rk = 0; rk < a.ksplit; ++rk)
       cluster_fail |= *static_cast<volatile int*>(__cluster_map_shared_rank((void*)abort_flag, (unsigned)rk));
     if (!cluster_fail) {
-      // CTA crank finishes weight rows [r0, r0 + per) of the tile.  Work item = (row,
-      // group of 4 real tokens): one float4 from every rank's partials, all loads in
-      // flight together, then up to 4 scalar stores.
-      const int per = TBN / a.ksplit;
-      const int r0 = (int)crank * per;
-      const int tg = (a.M + 3) >> 2;
-      const float4* src[kMaxCluster];
+      const int per4 = TBN / a.ksplit / 4;  // groups of 4 rows finished by this CTA
+      const int r0 = (int)crank * (TBN / a.ksplit);
+      const float* src[kMaxCluster];
 #pragma unroll
       for (int rk = 0; rk < kMaxCluster; ++rk)
-        src[rk] = static_cast<const float4*>(__cluster_map_shared_rank((void*)part, (unsigned)(rk < a.ksplit ? rk : 0)));
-      for (int it = tid; it < per * tg; it += kTmaThreads) {
-        const int rr = r0 + it / tg, g = it % tg;
+        src[rk] = static_cast<const float*>(__cluster_map_shared_rank((void*)part, (unsigned)(rk < a.ksplit ? rk : 0)));
+      for (int it = tid; it < a.M * per4; it += kTokThreads) {
+        const int mm = it / per4, c = r0 + 4 * (it % per4);
         float4 v[kMaxCluster];
 #pragma unroll
         for (int rk = 0; rk < kMaxCluster; ++rk)
-          v[rk] = rk < a.ksplit ? src[rk][(size_t)rr * 32 + g] : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[rk] = rk < a.ksplit ? *reinterpret_cast<const float4*>(src[rk] + (size_t)mm * kPartStride + c)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
         int acc[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int rk = 0; rk < kMaxCluster; ++rk) {
           acc[0] += __float2int_rn(v[rk].x); acc[1] += __float2int_rn(v[rk].y);
           acc[2] += __float2int_rn(v[rk].z); acc[3] += __float2int_rn(v[rk].w);
         }
-        const int n = n0 + rr;
-        if (n < a.N) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int mm = 4 * g + q;
-            if (mm < a.M) {
-              a.y[(size_t)mm * a.N + n] = dequant(acc[q], scale[128 + mm], gam, scale[mm]);
-              if (a.acc_out) a.acc_out[(size_t)mm * a.N + n] = acc[q];
-            }
-          }
-        }
+        store4(mm, n0 + c, acc[0], acc[1], acc[2], acc[3]);
       }
     }
     cluster_sync();  // no CTA leaves while others still read its shared memory
@@ -862,31 +859,34 @@ __device__ __forceinline__ void tok_epilogue(const Args& a, uint32_t tmem, float
     for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
       uint32_t v[32];
       tmem_ld32(taddr + (uint32_t)c0, v);
-      int acc[32];
+      if (m < a.M) {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) acc[t] = __float2int_rn(__uint_as_float(v[t]));
-      store_run(n0 + c0, acc, 32);
+        for (int t = 0; t < 32; t += 4)
+          store4(m, n0 + c0 + t, __float2int_rn(__uint_as_float(v[t])), __float2int_rn(__uint_as_float(v[t + 1])),
+                 __float2int_rn(__uint_as_float(v[t + 2])), __float2int_rn(__uint_as_float(v[t + 3])));
+      }
     }
   }
   if (tid == 0 && cluster_fail) atomicExch(&g_gemm_status, (int)TW_ERR_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(kTokThreads, 1)
     gemm_tok_kernel(const __grid_constant__ CUtensorMap mapX, Args a) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw0 = smem_u32(smem_raw);
   const uint32_t base = (raw0 + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw0);
-  const int NS = a.nstages;
-  const uint32_t op_bytes = TA_STAGE + TB_STAGE;  // 48 KB: activations, then weights
-  const uint32_t op0 = base;
-  const uint32_t wraw = base + (uint32_t)NS * op_bytes;  // [kTokARing][256 rows][16 B]
+  const uint32_t a0 = base;                                         // [kTokNA][16 KB] activations
+  const uint32_t b0 = a0 + (uint32_t)kTokNA * TA_STAGE;             // [kTokNB][32 KB] widened weights
+  const uint32_t wraw = b0 + (uint32_t)kTokNB * TB_STAGE;           // [kTokARing][256 rows][16 B]
   unsigned char* ctrl = gbase + a.ctrl_off;
-  const uint32_t op_full = smem_u32(ctrl);  // [kMaxStages]
-  const uint32_t op_empty = op_full + 8 * kMaxStages;
-  const uint32_t bar_done = op_empty + 8 * kMaxStages;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctrl + 16 * kMaxStages + 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 16 * kMaxStages + 12);
+  const uint32_t a_full = smem_u32(ctrl);                            // [kTokNA]
+  const uint32_t a_empty = a_full + 8 * kTokNA;
+  const uint32_t b_full = a_empty + 8 * kTokNA;                      // [kTokNB]
+  const uint32_t b_empty = b_full + 8 * kTokNB;
+  const uint32_t bar_done = b_empty + 8 * kTokNB;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctrl + 16 * (kTokNA + kTokNB) + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 16 * (kTokNA + kTokNB) + 12);
   float* scale = reinterpret_cast<float*>(ctrl + kScaleOff);  // [128] s_x, [128] dequantisation scales
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -896,9 +896,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const int nk = max(0, min(a.kstages_per_split, a.K / BK - kst0));
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(op_full + 8 * s, kTmaConv / 32 + 1);
-      mbar_init(op_empty + 8 * s, 1);
+    for (int s = 0; s < kTokNA; ++s) {
+      mbar_init(a_full + 8 * s, 1);
+      mbar_init(a_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < kTokNB; ++s) {
+      mbar_init(b_full + 8 * s, kTmaConv / 32);
+      mbar_init(b_empty + 8 * s, 1);
     }
     mbar_init(bar_done, 1);
     *abort_flag = 0;
@@ -916,24 +920,27 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
+  pdl_trigger();
 
   if (warp == 8) {
     // ------------------------------------------------------------ activation tiles
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapX)) : "memory");
+      pdl_wait_all();  // the widened activations come from the kernel in front
       int issued = 0;
       for (int i = 0; i < nk; ++i) {
-        const int s = i % NS;
-        if (i >= NS && !mbar_wait(op_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag)) {
+        const int s = i % kTokNA;
+        if (i >= kTokNA && !mbar_wait(a_empty + 8 * s, (uint32_t)(((i / kTokNA) - 1) & 1), abort_flag)) {
           ok = false;
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(op_full + 8 * s, (uint32_t)TA_STAGE);
-        tma_load_2d(op0 + (uint32_t)s * op_bytes, &mapX, (kst0 + i) * BK, 0, op_full + 8 * s);
+        mbar_arrive_expect_tx(a_full + 8 * s, (uint32_t)TA_STAGE);
+        tma_load_2d(a0 + (uint32_t)s * TA_STAGE, &mapX, (kst0 + i) * BK, 0, a_full + 8 * s);
         issued = i + 1;
       }
-      for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(op_full + 8 * (i % NS), (uint32_t)((i / NS) & 1));
+      for (int i = max(0, issued - kTokNA); i < issued; ++i)
+        mbar_wait(a_full + 8 * (i % kTokNA), (uint32_t)((i / kTokNA) & 1));
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -941,29 +948,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TBN >> 3) << 17) | ((128u >> 4) << 24);
       for (int i = 0; i < nk; ++i) {
-        const int s = i % NS;
-        if (!mbar_wait(op_full + 8 * s, (uint32_t)((i / NS) & 1), abort_flag) || *abort_flag) {
+        const int sa = i % kTokNA, sb = i % kTokNB;
+        if (!mbar_wait(a_full + 8 * sa, (uint32_t)((i / kTokNA) & 1), abort_flag) ||
+            !mbar_wait(b_full + 8 * sb, (uint32_t)((i / kTokNB) & 1), abort_flag) || *abort_flag) {
           ok = false;
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t As = op0 + (uint32_t)s * op_bytes, Bs = As + TA_STAGE;
+        const uint32_t As = a0 + (uint32_t)sa * TA_STAGE, Bs = b0 + (uint32_t)sb * TB_STAGE;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           mma_bf16(tmem, sw128_desc(As + 32 * kk), sw128_desc(Bs + 32 * kk), idesc, (i | kk) ? 1u : 0u);
-        mma_commit(op_empty + 8 * s);
+        mma_commit(a_empty + 8 * sa);
+        mma_commit(b_empty + 8 * sb);
       }
       mma_commit(bar_done);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ weight converters (warps 0-7)
-    for (int j = tid; j < 128; j += kTmaConv) {
-      const float sm = j < a.M ? __ldg(a.s_x + j) : 0.0f;
-      scale[j] = sm;
-      scale[128 + j] = dequant_scale(__ldg(a.w_scale), sm);
-    }
     const int r = tid;  // weight row of the tile owned by this thread
     const bool rowv = n0 + r < a.N;
     const uint8_t* gW = a.packed + (size_t)(rowv ? n0 + r : 0) * (a.K / 4);
@@ -977,12 +981,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
 #pragma unroll
-    for (int i = 0; i < kTokARing; ++i) fetch(i);
+    for (int i = 0; i < kTokARing; ++i) fetch(i);  // weights never depend on the kernel in front
+    for (int j = tid; j < 128; j += kTmaConv) {     // s_x was written two kernels back
+      const float sm = j < a.M ? __ldg(a.s_x + j) : 0.0f;
+      scale[j] = sm;
+      scale[128 + j] = dequant_scale(__ldg(a.w_scale), sm);
+    }
     for (int i = 0; i < nk; ++i) {
-      const int s = i % NS;
+      const int s = i % kTokNB;
       asm volatile("cp.async.wait_group %0;" ::"n"(kTokARing - 1) : "memory");
       int okw = 1;
-      if (lane == 0) okw = i < NS || mbar_wait(op_empty + 8 * s, (uint32_t)(((i / NS) - 1) & 1), abort_flag);
+      if (lane == 0) okw = i < kTokNB || mbar_wait(b_empty + 8 * s, (uint32_t)(((i / kTokNB) - 1) & 1), abort_flag);
       okw = __shfl_sync(0xffffffffu, okw, 0);
       __syncwarp();
       if (!okw) {
@@ -996,7 +1005,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                    : "r"(rslot + (uint32_t)(i % kTokARing) * TW_RAW));
       if (!rowv) w = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
       fetch(i + kTokARing);
-      const uint32_t Bs = op0 + (uint32_t)s * op_bytes + TA_STAGE;
+      const uint32_t Bs = b0 + (uint32_t)s * TB_STAGE;
       const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -1007,11 +1016,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(op_full + 8 * s);
+      if (lane == 0) mbar_arrive(b_full + 8 * s);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
+  pdl_wait_all();  // every thread stores outputs: the kernel in front must have finished
   const bool done_ok = mbar_wait(bar_done, 0);
   tc_fence_after();
   __syncthreads();
@@ -1028,11 +1038,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
 }
 
-
 // x_q [M][K] int8 -> bf16 [M][K], each 16-element group in the MMA K order
 // 0,4,1,5,2,6,3,7,8,12,9,13,10,14,11,15 (the order widen_codes gives the weights).
 __global__ void __launch_bounds__(256) widen_acts_kernel(const int8_t* __restrict__ x_q, long long groups,
                                                          uint4* __restrict__ out) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the GEMM behind may start fetching weights
   const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
   uint4 lo, hi;
@@ -1166,15 +1176,9 @@ bool gemm_tok_plan(int M, int N, int K, int num_sms, GemmPlan& p) {
   while (p.ksplit < kMaxCluster && (long long)p.tiles_n * (p.ksplit * 2) <= num_sms && nkst / (p.ksplit * 2) >= 8)
     p.ksplit *= 2;
   p.kstages_per_split = (nkst + p.ksplit - 1) / p.ksplit;
-  const size_t op = (size_t)TA_STAGE + TB_STAGE;
-  const size_t fixed = (size_t)kTokARing * TW_RAW;
-  int ns = (int)((200 * 1024 - fixed) / op);
-  if (ns > kMaxStages) ns = kMaxStages;
-  if (ns > p.kstages_per_split) ns = p.kstages_per_split < 2 ? 2 : p.kstages_per_split;
-  if (ns < 2) return false;
-  p.nstages = ns;
-  size_t body = (size_t)ns * op + fixed;
-  const size_t partial = (size_t)TBN * 128 * 4;
+  p.nstages = kTokNA;
+  size_t body = (size_t)kTokNA * TA_STAGE + (size_t)kTokNB * TB_STAGE + (size_t)kTokARing * TW_RAW;
+  const size_t partial = (size_t)128 * kPartStride * 4;
   if (p.ksplit > 1 && body < partial) body = partial;
   p.ctrl_off = (uint32_t)body;
   p.smem = 1024 + body + kCtrlBytes;
@@ -1209,16 +1213,18 @@ cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const in
       if (e != cudaSuccess) return e;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)(tp.tiles_n * tp.ksplit), 1);
-      cfg.blockDim = dim3(kTmaThreads);
+      cfg.blockDim = dim3(kTokThreads);
       cfg.dynamicSmemBytes = tp.smem;
       cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
+      cudaLaunchAttribute attr[2];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = (unsigned)tp.ksplit;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
-      cfg.numAttrs = 1;
+      cfg.numAttrs = 2;
       return cudaLaunchKernelEx(&cfg, gemm_tok_kernel, mapX, a);
     }
   }
