@@ -19,9 +19,12 @@ value   = algorithmic bytes of all GEMVs in the step (packed weights + int8 acti
           + scales) / device time of the step, whole job (all ranks).
 e2e     = the same metric with the step's inputs copied from pinned host memory and all
           outputs copied back inside the timed region (one copy each way).
-roofline: the GEMV kernel; per-launch durations from CUDA events around each GEMV launch
-          of extra steps enqueued behind a short GPU sleep (so host launch overhead does
-          not show), bytes per launch from the shapes; peak = measured HBM copy rate.
+roofline: the product kernel.  Average launch duration = the timed region's device time
+          over its product launches (fused path: every launch of the step); otherwise a graph
+          of the product calls alone, replayed like the timed region.  Algorithmic bytes (or
+          integer ops, M > 16) per launch = the step's over its launches; peak = measured HBM
+          copy rate (or bf16 tensor rate).  traffic = DRAM bytes per launch from the committed
+          ncu summary when it was taken on the unchanged kernel, else null.
 cpu_baseline / --impl reference: the CPU oracle (oracle/), as it stands, on the host.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling,
@@ -60,7 +63,7 @@ WORKLOADS = {
 SHAPE_TEXT = {"2B": "hidden 2560, ffn 6912, 20/5 heads", "8B": "hidden 4096, ffn 14336, 32/8 heads",
               "70B": "hidden 8192, ffn 28672, 64/8 heads"}
 GEMV_SOURCES = ["ternary_weight_quant_b300/csrc/tw_gemv_stream.cu", "ternary_weight_quant_b300/csrc/tw_common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_dram_traffic.json")
+TRAFFIC_FILES = {"2b": os.path.join(ROOT, "profiles", "gemv_stream_2b_layer_launches.md")}
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -141,15 +144,24 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per GEMV launch from the committed ncu summary, if the kernel is unchanged."""
-    if not os.path.exists(TRAFFIC_FILE):
+def recorded_traffic(workload):
+    """DRAM bytes per launch (read + write, averaged over a step's launches) from the committed
+    ncu summary of this workload, if it was taken on the current kernel sources."""
+    path = TRAFFIC_FILES.get(workload)
+    if path is None or not os.path.exists(path):
         return None
-    with open(TRAFFIC_FILE) as f:
-        d = json.load(f)
-    if d.get("source_hash") != source_hash(GEMV_SOURCES):
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ": " in line:
+                k, v = line[2:].split(": ", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_hash") != source_hash(GEMV_SOURCES):
         return None
-    return d.get("bytes_per_step_launch_avg")
+    try:
+        return float(fields["dram_bytes_per_launch_avg"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -355,18 +367,20 @@ class DecodeStack:
                 self._fused_ok[key] = False
         return self._fused_ok[key]
 
-    def enqueue(self, events=None, fused=True):
+    def enqueue(self, events=None, fused=True, product_only=False):
         """Enqueue one step on the current stream (optionally with events around each GEMV).
 
         fused: one tw_quant_gemv launch per GEMV (quantisation fused in, programmatic
-        dependent launch); otherwise tw_rmsnorm_quant_act / tw_quant_act + tw_ternary_gemv."""
+        dependent launch); otherwise tw_rmsnorm_quant_act / tw_quant_act + tw_ternary_gemv.
+        product_only: leave the separate quantisation kernels out (their outputs from an
+        earlier step stay in place), so that the product calls can be timed on their own."""
         import seeded_inputs as si
         tw = self.tw
         for d in self.L:
             for name, N, K, pro in self.plan:
                 e = d[name]
                 fz = fused and self.fused_ok(e)
-                if not fz:
+                if not fz and not product_only:
                     if pro == "rms":
                         tw.tw_rmsnorm_quant_act(e["x"], e["g"], si.RMS_EPS, e["x_q"], e["s_x"], e["x_sum"])
                     else:
@@ -395,18 +409,32 @@ def gpu_sleep(ms: float):
     torch.cuda._sleep(int(ms * 2.0e6))
 
 
-def capture(stack, fused):
+def capture(stack, fused, product_only=False):
     import torch
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        stack.enqueue(fused=fused)
+        stack.enqueue(fused=fused, product_only=product_only)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        stack.enqueue(fused=fused)
+        stack.enqueue(fused=fused, product_only=product_only)
     return graph
+
+
+def timed_replays(graph, steps, world):
+    """Seconds for `steps` replays of `graph`, CUDA events on the replaying stream."""
+    import torch
+    start, stop = events_new(), events_new()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(steps):
+        graph.replay()
+    stop.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / 1e3
 
 
 def run_ours(args):
@@ -448,7 +476,32 @@ def run_ours(args):
     ms_per_step = elapsed_max / args.steps * 1e3
     us_per_layer = ms_per_step * 1e3 / layers
 
-    # ---- roofline of the product kernel: events around each product launch of extra steps
+    # ---- roofline of the product kernel.  Fused: every launch of the step is the product
+    # kernel, so its average launch duration is the timed region over its launches.  Otherwise
+    # a second graph holds only the product calls (the quantised inputs stay from earlier
+    # steps) and is replayed as many times as the timed region, timed the same way.
+    shapes = {name: (N, K) for name, N, K, _ in plan}
+    peak_hbm, peak_kind = measured_peaks()
+    prod_calls_per_step = layers * len(plan)
+    whole_step = fused and all(stack.fused_ok(stack.L[0][n]) for n in shapes)
+    if whole_step:
+        prod_elapsed = elapsed
+    else:
+        pgraph = capture(stack, fused, product_only=True)
+        for _ in range(args.warmup):
+            pgraph.replay()
+        prod_elapsed = timed_replays(pgraph, args.steps, world)
+    avg_launch_s = prod_elapsed / (args.steps * prod_calls_per_step)
+    if M <= 16:
+        algo_per_call = bytes_per_step / prod_calls_per_step
+        achieved, peak, unit, bound = algo_per_call / avg_launch_s / 1e9, peak_hbm, "GB/s", "hbm"
+    else:
+        algo_per_call = ops_per_step / prod_calls_per_step
+        peak, pk = measured_tensor_peak()
+        achieved, unit, bound, peak_kind = algo_per_call / avg_launch_s / 1e12, "TFLOP/s", "tensor", pk
+
+    # per shape, each call on its own: events around each product call of extra steps enqueued
+    # behind a short GPU sleep (host launch overhead hidden; no overlap with the next call)
     per_launch = {}
     for rep in range(3):
         evs = []
@@ -459,17 +512,6 @@ def run_ours(args):
             continue
         for name, a, b in evs:
             per_launch.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
-    prod_time = sum(sum(v) for v in per_launch.values())
-    prod_launches = sum(len(v) for v in per_launch.values())
-    shapes = {name: (N, K) for name, N, K, _ in plan}
-    peak_hbm, peak_kind = measured_peaks()
-    if M <= 16:
-        algo = sum(gemv_bytes(*shapes[n], M) * len(v) for n, v in per_launch.items())
-        achieved, peak, unit, bound = algo / prod_time / 1e9, peak_hbm, "GB/s", "hbm"
-    else:
-        algo = sum(2 * M * shapes[n][0] * shapes[n][1] * len(v) for n, v in per_launch.items())
-        peak, pk = measured_tensor_peak()
-        achieved, unit, bound, peak_kind = algo / prod_time / 1e12, "TFLOP/s", "tensor", pk
     per_shape = {n: {"bytes": gemv_bytes(*shapes[n], M), "us_median": statistics.median(v) * 1e6,
                      "GB/s": gemv_bytes(*shapes[n], M) / statistics.median(v) / 1e9,
                      "TFLOP/s": 2 * M * shapes[n][0] * shapes[n][1] / statistics.median(v) / 1e12}
@@ -537,9 +579,14 @@ def run_ours(args):
             "pct_of_nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
             "pct_of_measured_copy": 100.0 * value / world / peak_hbm,
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                         "frac": achieved / peak, "traffic": recorded_traffic() if fused else None,
+                         "frac": achieved / peak,
+                         "traffic": recorded_traffic(args.workload) if fused else None,
                          "kernel": kern, "peak_source": peak_kind,
-                         "launches_timed": prod_launches, "per_shape": per_shape},
+                         "algorithmic_per_launch": algo_per_call,
+                         "avg_launch_us": avg_launch_s * 1e6,
+                         "timing": ("timed region / product launches" if whole_step else
+                                    "graph of the product calls only, replayed like the timed region"),
+                         "per_shape_isolated": per_shape},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches * args.steps,

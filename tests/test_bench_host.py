@@ -66,3 +66,17 @@ def test_step_bytes_match_layer_shapes():
     acts = 2560 * 3 + 6912
     scales = 4 * (4 + 4)
     assert bench.step_bytes(1) == 30 * (packed + acts + scales)
+
+
+def test_recorded_traffic_needs_matching_source_hash(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    f = tmp_path / "traffic.md"
+    monkeypatch.setitem(bench.TRAFFIC_FILES, "2b", str(f))
+    assert bench.recorded_traffic("2b") is None  # no summary
+    f.write_text("# summary\n- source_hash: `%s`\n- dram_bytes_per_launch_avg: 4321.5\n"
+                 % bench.source_hash(bench.GEMV_SOURCES))
+    assert bench.recorded_traffic("2b") == 4321.5
+    f.write_text("- source_hash: `0000000000000000`\n- dram_bytes_per_launch_avg: 4321.5\n")
+    assert bench.recorded_traffic("2b") is None  # taken on another kernel
+    assert bench.recorded_traffic("8b_m1") is None
