@@ -6,8 +6,9 @@
 //   [RMSNorm] r = exact sum of x^2 (128-bit fixed point relative to the row's
 //             largest exponent; rows with a wider exponent spread use a histogram
 //             of 48-bit squared mantissas per exponent), rounded once to double,
-//             ms = (float)(r / K), inv = 1 / sqrt(ms + eps) (IEEE fp32 sqrt and
-//             divide), u = fl(fl(x * inv) * g);
+//             ms = (float)(r / K) (the double division emulated with integers),
+//             inv = 1 / sqrt(ms + eps) (IEEE fp32 sqrt and divide),
+//             u = fl(fl(x * inv) * g);
 //   a = max |u|;  x_q = clamp(rne(fl(fl(u * 127) / a)), -128, 127);  s_x = a;
 //   x_sum = sum x_q.
 // All fp32 steps use the _rn intrinsics, so no contraction or approximate
@@ -18,7 +19,7 @@ namespace tw {
 
 template <bool RMS>
 __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict__ x,
-                                                        const float* __restrict__ g, float eps, int K,
+                                                        const float* __restrict__ g, float eps, int K, KDiv kd,
                                                         int8_t* __restrict__ x_q, float* __restrict__ s_x,
                                                         int32_t* __restrict__ x_sum) {
   const int m = blockIdx.x;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict_
         Sum128 t;
         t.lo = t.hi = 0ull;
         for (int w = 0; w < nwarps; ++w) sum128_add(t, red_lo[w], red_hi[w]);
-        sh_inv = rms_inv(sum128_to_double(t, E), K, eps);
+        sh_inv = rms_inv_sum128(t, E, kd, eps);
       }
     } else {
       // exponents spread too far for 128 bits: exact exponent-bucket histogram
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict_
       __syncthreads();
       if (warp == 0) {
         const double r = warp_exact_hist_to_double(hist, 256, 2, -298);
-        if (lane == 0) sh_inv = rms_inv(r, K, eps);
+        if (lane == 0) sh_inv = rms_inv(r, kd, eps);
       }
     }
     __syncthreads();
@@ -181,13 +182,13 @@ static int act_threads(long long K) {
 
 cudaError_t tw_launch_quant_act(const float* x, long long M, long long K, int8_t* x_q, float* s_x,
                                 int32_t* x_sum, cudaStream_t stream) {
-  tw::act_quant_kernel<false><<<(unsigned)M, act_threads(K), 0, stream>>>(x, nullptr, 0.0f, (int)K, x_q, s_x,
+  tw::act_quant_kernel<false><<<(unsigned)M, act_threads(K), 0, stream>>>(x, nullptr, 0.0f, (int)K, tw::make_kdiv((int)K), x_q, s_x,
                                                                          x_sum);
   return cudaGetLastError();
 }
 
 cudaError_t tw_launch_rmsnorm_quant_act(const float* x, const float* g, float eps, long long M, long long K,
                                         int8_t* x_q, float* s_x, int32_t* x_sum, cudaStream_t stream) {
-  tw::act_quant_kernel<true><<<(unsigned)M, act_threads(K), 0, stream>>>(x, g, eps, (int)K, x_q, s_x, x_sum);
+  tw::act_quant_kernel<true><<<(unsigned)M, act_threads(K), 0, stream>>>(x, g, eps, (int)K, tw::make_kdiv((int)K), x_q, s_x, x_sum);
   return cudaGetLastError();
 }

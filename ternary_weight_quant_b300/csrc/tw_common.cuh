@@ -1,6 +1,7 @@
 // tw_common.cuh -- small device helpers shared by the libtw kernels (sm_103a).
 #pragma once
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "../../include/ternary_w158a8.h"
@@ -123,7 +124,7 @@ struct Sum128 {
   unsigned long long lo, hi;
 };
 
-__device__ __forceinline__ void sum128_add(Sum128& s, unsigned long long lo, unsigned long long hi) {
+__host__ __device__ __forceinline__ void sum128_add(Sum128& s, unsigned long long lo, unsigned long long hi) {
   const unsigned long long t = s.lo + lo;
   s.hi += hi + (t < s.lo ? 1ull : 0ull);
   s.lo = t;
@@ -148,32 +149,287 @@ __device__ __forceinline__ Sum128 sum128_shfl_xor(const Sum128& s, int o) {
   return r;
 }
 
-// (hi * 2^64 + lo) * 2^(2E - 364), rounded once to the nearest double (ties to even).
-// The result is always a normal double (its exponent is at least -362), so it is
-// assembled from its bits: a 53-bit significand m in [2^52, 2^53] is added to the
-// biased exponent field minus one, which also carries m = 2^53 into the exponent.
-__device__ __forceinline__ double sum128_to_double(const Sum128& s, int E) {
-  if (s.hi == 0ull && s.lo == 0ull) return 0.0;
-  const unsigned __int128 v = ((unsigned __int128)s.hi << 64) | s.lo;
-  const int n = s.hi ? 128 - __clzll((long long)s.hi) : 64 - __clzll((long long)s.lo);  // bit length
-  unsigned long long m;
-  if (n <= 53) {
-    m = (unsigned long long)v << (53 - n);
-  } else {
-    const int drop = n - 53;
-    m = (unsigned long long)(v >> drop);
-    const unsigned __int128 rem = v & (((unsigned __int128)1 << drop) - 1);
-    const unsigned __int128 half = (unsigned __int128)1 << (drop - 1);
-    if (rem > half || (rem == half && (m & 1ull))) m += 1ull;
+// Shift of a Sum128 right by sh bits (0 <= sh), reporting whether a nonzero bit
+// fell off: used to bring a sum taken relative to a smaller exponent E' into the
+// units 2^(2E - 364) of a larger one (sh = 2 (E - E')).
+__host__ __device__ __forceinline__ bool sum128_shr_exact(Sum128& s, int sh) {
+  if (sh == 0) return true;
+  if (sh >= 128) {
+    const bool ok = (s.lo | s.hi) == 0ull;
+    s.lo = s.hi = 0ull;
+    return ok;
   }
-  const long long eb = (long long)(n - 1 + 2 * E - 364) + 1023;  // biased exponent of the leading bit
-  return __longlong_as_double((long long)(((unsigned long long)(eb - 1) << 52) + m));
+  const unsigned __int128 v = ((unsigned __int128)s.hi << 64) | s.lo;
+  const unsigned __int128 r = v >> sh;
+  s.lo = (unsigned long long)r;
+  s.hi = (unsigned long long)(r >> 64);
+  return (r << sh) == v;
 }
 
-// 1 / sqrt(fl32(r / K) + eps) with IEEE fp32 square root and divide; r / K in double.
-__device__ __forceinline__ float rms_inv(double r, int K, float eps) {
-  const float ms = __double2float_rn(__ddiv_rn(r, (double)K));
+__host__ __device__ __forceinline__ int clz64(unsigned long long v) {
+#ifdef __CUDA_ARCH__
+  return __clzll((long long)v);
+#else
+  return v ? __builtin_clzll(v) : 64;
+#endif
+}
+
+// (hi * 2^64 + lo) * 2^(2E - 364) > 0 rounded once to double precision (nearest,
+// ties to even), returned as m * 2^e with 2^52 <= m <= 2^53 (m = 2^53 when the
+// rounding carries).
+__host__ __device__ __forceinline__ void sum128_round53(const Sum128& s, int E, unsigned long long& m, int& e) {
+  const unsigned __int128 v = ((unsigned __int128)s.hi << 64) | s.lo;
+  const int n = s.hi ? 128 - clz64(s.hi) : 64 - clz64(s.lo);  // bit length
+  if (n <= 53) {
+    m = (unsigned long long)v << (53 - n);
+    e = 2 * E - 364 - (53 - n);
+    return;
+  }
+  const int drop = n - 53;
+  m = (unsigned long long)(v >> drop);
+  const unsigned __int128 rem = v & (((unsigned __int128)1 << drop) - 1);
+  const unsigned __int128 half = (unsigned __int128)1 << (drop - 1);
+  if (rem > half || (rem == half && (m & 1ull))) m += 1ull;
+  e = 2 * E - 364 + drop;
+}
+
+// The same value as a double.  It is always normal (its exponent is at least -362),
+// so it is assembled from its bits: m in [2^52, 2^53] added to the biased exponent
+// field minus one also carries m = 2^53 into the exponent.
+__device__ __forceinline__ double sum128_to_double(const Sum128& s, int E) {
+  if (s.hi == 0ull && s.lo == 0ull) return 0.0;
+  unsigned long long m;
+  int e;
+  sum128_round53(s, E, m, e);
+  return __longlong_as_double((long long)(((unsigned long long)(e + 52 + 1023 - 1) << 52) + m));
+}
+
+// Division by the row length K (1 <= K <= 2^16) by multiplication with an
+// invariant-integer reciprocal (Granlund and Montgomery, "Division by invariant
+// integers using multiplication", 1994, Theorem 4.2): with l = ceil(log2 K) and
+// mk = ceil(2^(54 + l) / K), floor(n / K) = floor(n * mk / 2^(54 + l)) for every
+// 0 <= n < 2^54, since 2^(54 + l) <= mk K <= 2^(54 + l) + K - 1 < 2^(54 + l) + 2^l.
+struct KDiv {
+  unsigned long long mk;
+  int sh;  // 54 + l
+  int K;
+};
+
+__host__ inline KDiv make_kdiv(int K) {
+  int l = 0;
+  while ((1 << l) < K) ++l;
+  const unsigned __int128 num = (unsigned __int128)1 << (54 + l);
+  KDiv d;
+  d.mk = (unsigned long long)((num + (unsigned __int128)(K - 1)) / (unsigned __int128)K);
+  d.sh = 54 + l;
+  d.K = K;
+  return d;
+}
+
+__host__ __device__ __forceinline__ unsigned long long kdiv_floor(unsigned long long n, const KDiv& d) {
+  return (unsigned long long)(((unsigned __int128)n * d.mk) >> d.sh);
+}
+
+// fl32(fl64(R / K)) for R = m * 2^e (2^52 <= m <= 2^53, R a normal double) with
+// integer arithmetic only: the quotient is formed to 32 more bits by two
+// invariant-integer divisions (the final remainder is the sticky bit), rounded to
+// nearest even at 53 bits, then rounded again at fp32 precision (normal or
+// subnormal), exactly as the two conversions of the double-precision formula.
+__host__ __device__ __forceinline__ float div_k_round_f32(unsigned long long m, int e, const KDiv& d) {
+  const unsigned long long K = (unsigned long long)d.K;
+  const unsigned long long q1 = kdiv_floor(m, d), r1 = m - q1 * K;
+  const unsigned long long t = r1 << 32;  // < 2^48
+  const unsigned long long q0 = kdiv_floor(t, d), r0 = t - q0 * K;
+  const unsigned __int128 q = ((unsigned __int128)q1 << 32) + q0;  // R / K = (q + r0 / K) 2^(e - 32)
+  const unsigned long long qh = (unsigned long long)(q >> 64), ql = (unsigned long long)q;
+  const int n = qh ? 128 - clz64(qh) : 64 - clz64(ql);  // >= 68
+  const int drop = n - 53;
+  unsigned long long mq = (unsigned long long)(q >> drop);
+  const unsigned __int128 rem = q & (((unsigned __int128)1 << drop) - 1);
+  const unsigned __int128 half = (unsigned __int128)1 << (drop - 1);
+  if (rem > half || (rem == half && (r0 != 0ull || (mq & 1ull)))) mq += 1ull;
+  const int eq = e - 32 + drop;  // fl64(R / K) = mq 2^eq, 2^52 <= mq <= 2^53
+  const int lead = 52 + eq + (int)(mq >> 53);  // exponent of its leading bit
+  uint32_t bits;
+  if (lead > 127) {
+    bits = 0x7f800000u;
+  } else if (lead >= -126) {
+    const int dr = (mq >> 53) ? 30 : 29;  // keep 24 bits
+    unsigned long long f = mq >> dr;
+    const unsigned long long rm = mq & ((1ull << dr) - 1), hf = 1ull << (dr - 1);
+    if (rm > hf || (rm == hf && (f & 1ull))) f += 1ull;  // f in [2^23, 2^24]
+    bits = ((uint32_t)(lead + 127 - 1) << 23) + (uint32_t)f;
+    if (bits > 0x7f800000u) bits = 0x7f800000u;
+  } else {
+    const int sh = -149 - eq;  // bits of mq below 2^-149, >= 30 here
+    if (sh >= 64) {
+      bits = 0u;
+    } else {
+      unsigned long long f = mq >> sh;
+      const unsigned long long rm = mq & ((1ull << sh) - 1), hf = 1ull << (sh - 1);
+      if (rm > hf || (rm == hf && (f & 1ull))) f += 1ull;
+      bits = (uint32_t)f;  // f = 2^23 is the smallest normal
+    }
+  }
+#ifdef __CUDA_ARCH__
+  return __uint_as_float(bits);
+#else
+  float out;
+  __builtin_memcpy(&out, &bits, 4);
+  return out;
+#endif
+}
+
+// ---------------------------------------------------------------------------
+// Sum of squares, fast path: float-float (unevaluated sum hi + lo of two fp32)
+// accumulation with error-free transformations (Knuth's TwoSum, the exact square
+// error v*v - fl(v*v) from one fused multiply-add, Dekker's Fast2Sum to
+// renormalise).  Every step keeps |lo| <= ulp(hi)/2 and loses at most about
+// 2^-45.5 of the running sum, so a row of up to 65532 elements summed by at most
+// 171 steps per thread and 9 tree levels is within 2^-37.5 of the exact sum S
+// (squares below 2^-126 add at most K 2^-149, negligible for the range admitted).
+// ff_mean_f32 then decides fl32(fl64(fl64(S) / K)) when that accuracy suffices
+// and reports failure otherwise (the caller takes the exact path).
+struct FF {
+  float hi, lo;
+};
+
+__host__ __device__ __forceinline__ float f_add(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fadd_rn(a, b);
+#else
+  return a + b;
+#endif
+}
+__host__ __device__ __forceinline__ float f_sub(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fsub_rn(a, b);
+#else
+  return a - b;
+#endif
+}
+__host__ __device__ __forceinline__ float f_mul(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fmul_rn(a, b);
+#else
+  return a * b;
+#endif
+}
+__host__ __device__ __forceinline__ float f_fma(float a, float b, float c) {
+#ifdef __CUDA_ARCH__
+  return __fmaf_rn(a, b, c);
+#else
+  return fmaf(a, b, c);
+#endif
+}
+__host__ __device__ __forceinline__ float f_div(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fdiv_rn(a, b);
+#else
+  return a / b;
+#endif
+}
+__host__ __device__ __forceinline__ uint32_t f_bits(float v) {
+#ifdef __CUDA_ARCH__
+  return __float_as_uint(v);
+#else
+  uint32_t b;
+  __builtin_memcpy(&b, &v, 4);
+  return b;
+#endif
+}
+__host__ __device__ __forceinline__ float f_from_bits(uint32_t b) {
+#ifdef __CUDA_ARCH__
+  return __uint_as_float(b);
+#else
+  float v;
+  __builtin_memcpy(&v, &b, 4);
+  return v;
+#endif
+}
+
+// hi + lo = a + b exactly (TwoSum, any order of magnitudes)
+__host__ __device__ __forceinline__ void ff_two_sum(float a, float b, float& hi, float& err) {
+  hi = f_add(a, b);
+  const float z = f_sub(hi, a);
+  err = f_add(f_sub(a, f_sub(hi, z)), f_sub(b, z));
+}
+
+__host__ __device__ __forceinline__ void ff_add_square(FF& s, float v) {
+  const float p = f_mul(v, v);
+  const float e = f_fma(v, v, -p);  // v*v - p exactly
+  float t, err;
+  ff_two_sum(s.hi, p, t, err);
+  const float lo = f_add(s.lo, f_add(err, e));
+  s.hi = f_add(t, lo);  // Fast2Sum: |t| >= |lo|
+  s.lo = f_sub(lo, f_sub(s.hi, t));
+}
+
+// Symmetric in its operands, so a butterfly leaves the same value in every lane.
+__host__ __device__ __forceinline__ void ff_add(FF& a, const FF& b) {
+  float t, err;
+  ff_two_sum(a.hi, b.hi, t, err);
+  const float lo = f_add(f_add(a.lo, b.lo), err);
+  a.hi = f_add(t, lo);
+  a.lo = f_sub(lo, f_sub(a.hi, t));
+}
+
+// ms = fl32(fl64(fl64(S) / K)) from s = hi + lo within 2^-37.5 S of S, with
+// ik = fl32(1 / K).  The quotient is formed as qh + ql: qh = fl(hi ik) (within
+// 2^-22.9 of hi / K), the remainder hi - qh K by one fused multiply-add (off by at
+// most 2^-47 hi), ql = fl(fl(r + lo) ik); qh + ql is within 2^-45 of S / K beyond the
+// error of s.  c = fl32(qh + ql) is the candidate, accepted when qh + ql lies farther
+// than 2^-35 c from both midpoints next to c: the exact quotient, and its two double
+// roundings, are then on the same side of them.  Sums outside [2^-80, 2^96] are
+// left to the exact path.
+__host__ __device__ __forceinline__ bool ff_mean_f32(const FF& s, int K, float ik, float& ms) {
+  if (!(s.hi >= 0x1p-80f && s.hi <= 0x1p96f)) return false;
+  const float kf = (float)K;
+  const float qh = f_mul(s.hi, ik);
+  const float r = f_fma(-qh, kf, s.hi);
+  const float ql = f_mul(f_add(r, s.lo), ik);
+  const float c = f_add(qh, ql);
+  const float d = f_add(f_sub(qh, c), ql);  // (qh + ql) - c
+  const uint32_t cb = f_bits(c);
+  const float up = f_sub(f_from_bits(cb + 1u), c), down = f_sub(c, f_from_bits(cb - 1u));
+  const float margin = f_mul(c, 0x1p-35f);
+  ms = c;
+  return f_add(d, margin) < f_mul(0.5f, up) && f_sub(d, margin) > f_mul(-0.5f, down);
+}
+
+// 1 / sqrt(ms + eps) with IEEE fp32 add, square root and divide.
+__host__ __device__ __forceinline__ float inv_rms_f32(float ms, float eps) {
+#ifdef __CUDA_ARCH__
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+#else
+  volatile float t = ms + eps;
+  return 1.0f / sqrtf(t);
+#endif
+}
+
+// RMSNorm scale from the exact sum of squares S = (hi:lo) 2^(2E - 364):
+// 1 / sqrt(fl32(fl64(S) / K) + eps), the division in double precision emulated
+// with integers (no double arithmetic).
+__host__ __device__ __forceinline__ float rms_inv_sum128(const Sum128& s, int E, const KDiv& d, float eps) {
+  float ms = 0.0f;
+  if (s.hi | s.lo) {
+    unsigned long long m;
+    int e;
+    sum128_round53(s, E, m, e);
+    ms = div_k_round_f32(m, e, d);
+  }
+  return inv_rms_f32(ms, eps);
+}
+
+// The same from a sum already rounded to double (the exact histogram path).
+__device__ __forceinline__ float rms_inv(double r, const KDiv& d, float eps) {
+  float ms = 0.0f;
+  if (r > 0.0) {
+    const unsigned long long b = (unsigned long long)__double_as_longlong(r);
+    const int be = (int)(b >> 52);  // r >= 2^-298: normal
+    ms = div_k_round_f32((b & ((1ull << 52) - 1)) | (1ull << 52), be - 1075, d);
+  }
+  return inv_rms_f32(ms, eps);
 }
 
 // round_half_even(fl32(p / a)) for a > 0 and |p| <= fl32(127 a), the same integer as

@@ -53,6 +53,8 @@ struct StreamArgs {
   const float* x;         // fused: fp32 activations [M][K] (NULL -> use x_q_in)
   const float* g;         // fused RMSNorm gain [K] or NULL
   float eps;
+  KDiv kd;                // invariant-integer division by K (RMSNorm mean, exact path)
+  float inv_k;            // fl32(1 / K) (RMSNorm mean, fast path)
   const int8_t* x_q_in;   // pre-quantised activations [M][K]
   const float* s_x_in;    // their scales [M]
   int M, N, K;
@@ -67,25 +69,7 @@ struct StreamArgs {
   int32_t* x_sum_out;
 };
 
-// Block-wide reductions of MT values (every thread gets the results).
-template <int MT>
-__device__ __forceinline__ void breduce_max_u32(uint32_t (&v)[MT], uint32_t* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    v[m] = __reduce_max_sync(0xffffffffu, v[m]);
-    if (lane == 0) red[warp * MT + m] = v[m];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    uint32_t t = red[m];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) t = max(t, red[w * MT + m]);
-    v[m] = t;
-  }
-  __syncthreads();
-}
+// Block-wide sum of MT values (every thread gets the results).
 template <int MT>
 __device__ __forceinline__ void breduce_sum_i32(int (&v)[MT], int* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -141,151 +125,83 @@ __device__ double row_sumsq_hist(const float4* xr, int K4, uint32_t (*limb)[256]
   return *out;
 }
 
-// Quantise the activations of MT tokens (after RMSNorm when RMS) into xs
-// (byte-transposed 16-element groups); scales to s_scale.  CTA 0 also stores
-// x_q, s_x and x_sum when asked.  When xf is not NULL the first pass copies x (and
-// the gain) into shared memory and the later passes read it from there.
-template <int MT, bool RMS>
-__device__ __forceinline__ void fused_prologue(const StreamArgs& a, uint4* xs, float* xf, float* s_scale,
-                                               uint32_t* red_u, int* red_i, unsigned long long* red_lo,
-                                               unsigned long long* red_hi, uint32_t (*limb)[256],
-                                               unsigned long long* hist, double* s_dbl, float* s_inv) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Quantisation of MT tokens into xs (byte-transposed 16-element groups): element k
+// of group k/16 goes to byte (k/4) % 4 of word k % 4 of that group.  u4 holds u
+// itself ([MT][K4]); with u4 == NULL, u = fl(fl(x * inv) * g) is recomputed from x
+// and g4.  CTA 0 also stores x_q, s_x and x_sum when asked.
+template <int MT>
+__device__ __forceinline__ void quantise_tokens(const StreamArgs& a, uint4* xs, const float4* u4, const float4* g4,
+                                                const float (&inv)[MT], const uint32_t (&am)[MT], int* red_i,
+                                                float* s_scale) {
+  const int tid = threadIdx.x;
   const int K = a.K, Kw = K >> 4, K4 = K >> 2;
-  const bool staged = xf != nullptr;
-  float4* xf4 = reinterpret_cast<float4*>(xf);  // [MT][K4] then the gain [K4]
-  const float4* g4 = staged && RMS ? xf4 + (size_t)MT * K4 : reinterpret_cast<const float4*>(a.g);
-  auto xsrc = [&](int m) -> const float4* {
-    return staged ? xf4 + (size_t)m * K4 : reinterpret_cast<const float4*>(a.x + (size_t)m * K);
-  };
-  // first pass: from global memory (staging copy), largest magnitude per token as bits
-  uint32_t mx[MT];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    mx[m] = 0u;
-    if (m < a.M) {
-      const float4* xg = reinterpret_cast<const float4*>(a.x + (size_t)m * K);
-      for (int i = tid; i < K4; i += kThreads) {
-        const float4 v = xg[i];
-        if (staged) xf4[(size_t)m * K4 + i] = v;
-        mx[m] = max(mx[m], max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
-                               max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
-      }
-    }
-  }
-  if (RMS && staged) {
-    const float4* gg = reinterpret_cast<const float4*>(a.g);
-    for (int i = tid; i < K4; i += kThreads) xf4[(size_t)MT * K4 + i] = gg[i];
-  }
-  breduce_max_u32<MT>(mx, red_u);  // its barriers also publish the staged copy
-  float inv[MT];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) inv[m] = 1.0f;
-  if constexpr (RMS) {
-    uint32_t wide[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      Sum128 sq;
-      sq.lo = sq.hi = 0ull;
-      bool wd = false;
-      const int E = max((int)(mx[m] >> 23), 1);
-      if (m < a.M) {
-        const float4* xr = xsrc(m);
-        for (int i = tid; i < K4; i += kThreads) {
-          const float4 v = xr[i];
-          sum128_add_square(sq, v.x, E, wd);
-          sum128_add_square(sq, v.y, E, wd);
-          sum128_add_square(sq, v.z, E, wd);
-          sum128_add_square(sq, v.w, E, wd);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const Sum128 t = sum128_shfl_xor(sq, o);
-        sum128_add(sq, t.lo, t.hi);
-      }
-      wide[m] = wd ? 1u : 0u;
-      if (lane == 0) {
-        red_lo[warp * MT + m] = sq.lo;
-        red_hi[warp * MT + m] = sq.hi;
-      }
-    }
-    breduce_max_u32<MT>(wide, red_u);  // its barrier also publishes red_lo / red_hi
-    // warp m combines the per-warp sums of token m; its lane 0 rounds the total and
-    // forms 1/sqrt(ms + eps) (double arithmetic is scarce on this part)
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m >= a.M) continue;
-      if (wide[m]) {
-        const double r = row_sumsq_hist(xsrc(m), K4, limb, hist, s_dbl);
-        if (tid == 0) s_inv[m] = rms_inv(r, K, a.eps);
-      } else if (warp == m) {
-        Sum128 t;
-        t.lo = lane < kWarps ? red_lo[lane * MT + m] : 0ull;
-        t.hi = lane < kWarps ? red_hi[lane * MT + m] : 0ull;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) {  // kWarps <= 16
-          const Sum128 u = sum128_shfl_xor(t, o);
-          sum128_add(t, u.lo, u.hi);
-        }
-        if (lane == 0) s_inv[m] = rms_inv(sum128_to_double(t, max((int)(mx[m] >> 23), 1)), K, a.eps);
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < MT; ++m) inv[m] = s_inv[m];
-  }
-  auto norm = [&](float v, float gg, int m) -> float { return RMS ? __fmul_rn(__fmul_rn(v, inv[m]), gg) : v; };
-  uint32_t am[MT];  // a = max |u| per token (u >= 0 compares as its bits)
-  if constexpr (RMS) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      am[m] = 0u;
-      if (m < a.M) {
-        const float4* xr = xsrc(m);
-        for (int i = tid; i < K4; i += kThreads) {
-          const float4 v = xr[i];
-          const float4 gg = g4[i];
-          const float t = fmaxf(fmaxf(fabsf(norm(v.x, gg.x, m)), fabsf(norm(v.y, gg.y, m))),
-                                fmaxf(fabsf(norm(v.z, gg.z, m)), fabsf(norm(v.w, gg.w, m))));
-          am[m] = max(am[m], __float_as_uint(t));
-        }
-      }
-    }
-    breduce_max_u32<MT>(am, red_u);
-  } else {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) am[m] = mx[m];  // without RMSNorm u = x: the first pass found max |x|
-  }
-  // quantise: thread by thread over 4-element units u (k = 4u .. 4u+3); element k of
-  // 16-element group k/16 goes to byte (k/4) % 4 of word k % 4 of that group in xs
   unsigned char* xsb = reinterpret_cast<unsigned char*>(xs);
   int qsum[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     qsum[m] = 0;
     const float amax = __uint_as_float(am[m]);
-    const float ra = amax > 0.0f ? __frcp_rn(amax) : 0.0f;
-    const float4* xr = xsrc(m);
-    for (int u = tid; u < K4; u += kThreads) {
-      uint32_t pq = 0u;
-      if (m < a.M) {
-        const float4 v = xr[u];
-        float4 gg = make_float4(1.f, 1.f, 1.f, 1.f);
-        if (RMS) gg = g4[u];
-        const float uu[4] = {norm(v.x, gg.x, m), norm(v.y, gg.y, m), norm(v.z, gg.z, m), norm(v.w, gg.w, m)};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          int t = amax > 0.0f ? quant_div(__fmul_rn(uu[e], 127.0f), amax, ra) : 0;
-          t = max(-128, min(127, t));
-          qsum[m] += t;
-          pq |= ((uint32_t)t & 0xffu) << (8 * e);
-        }
-        if (blockIdx.x == 0 && a.x_q_out) reinterpret_cast<uint32_t*>(a.x_q_out + (size_t)m * K)[u] = pq;
+    // d = fl(p ra) with ra within one ulp of 1 / a (rcp.approx, documented to 1 ulp)
+    // is within |p/a| 2^-22 < 3.1e-5 of p / a (|p/a| <= 127), and fl32(p/a) within
+    // 2^-18 of it: when d is at least 5e-5 from a half-integer, rint(d) is
+    // round_half_even(fl32(p / a)).  Units with an element nearer than that, or with
+    // a non-finite d (ra is NaN when a lies outside [2^-120, 2^120]), are redone with
+    // the IEEE divide.
+    float ra = amax == 0.0f ? 0.0f : __int_as_float(0x7fffffff);
+    if (amax >= 0x1p-120f && amax <= 0x1p120f) asm("rcp.approx.f32 %0, %1;" : "=f"(ra) : "f"(amax));
+    const float4* ur = u4 ? u4 + (size_t)m * K4 : reinterpret_cast<const float4*>(a.x + (size_t)m * K);
+    auto load_u = [&](int u) -> float4 {
+      float4 v = ur[u];
+      if (!u4) {
+        const float4 gg = g4[u];
+        v = make_float4(__fmul_rn(__fmul_rn(v.x, inv[m]), gg.x), __fmul_rn(__fmul_rn(v.y, inv[m]), gg.y),
+                        __fmul_rn(__fmul_rn(v.z, inv[m]), gg.z), __fmul_rn(__fmul_rn(v.w, inv[m]), gg.w));
       }
-      unsigned char* gb = xsb + (size_t)m * Kw * 16 + (u >> 2) * 16 + (u & 3);
+      return v;
+    };
+    // round to nearest even without conversion instructions: for |d| < 2^22,
+    // d + 1.5 2^23 rounds d to an integer held in the low mantissa bits
+    auto q_fast = [&](float uv, bool& near) -> uint32_t {
+      const float d = __fmul_rn(__fmul_rn(uv, 127.0f), ra);
+      const float sb = __fadd_rn(d, 12582912.0f);
+      const float r = __fsub_rn(sb, 12582912.0f);
+      near |= !(fabsf(__fsub_rn(d, r)) < 0.49995f);  // also when d is not finite
+      const int t = (int)(__float_as_uint(sb) & 0x7fffffu) - 0x400000;
+      return (uint32_t)max(-128, min(127, t)) & 0xffu;
+    };
+    auto q_exact = [&](float uv) -> uint32_t {
+      const int t = amax > 0.0f ? __float2int_rn(__fdiv_rn(__fmul_rn(uv, 127.0f), amax)) : 0;
+      return (uint32_t)max(-128, min(127, t)) & 0xffu;
+    };
+    if (m < a.M) {
+      // warp-uniform trip count (lane l takes unit base + l), so the vote below is safe
+#pragma unroll 2
+      for (int base = (tid & ~31); base < K4; base += kThreads) {
+        const int u = base + (tid & 31);
+        uint32_t pq = 0u;
+        bool near = false;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (u < K4) {
+          v = load_u(u);
+          pq = q_fast(v.x, near) | (q_fast(v.y, near) << 8) | (q_fast(v.z, near) << 16) | (q_fast(v.w, near) << 24);
+        }
+        if (__any_sync(0xffffffffu, near) && near)  // rare
+          pq = q_exact(v.x) | (q_exact(v.y) << 8) | (q_exact(v.z) << 16) | (q_exact(v.w) << 24);
+        if (u < K4) {
+          qsum[m] += (int)(int8_t)(pq & 0xffu) + (int)(int8_t)((pq >> 8) & 0xffu) +
+                     (int)(int8_t)((pq >> 16) & 0xffu) + (int)(int8_t)(pq >> 24);
+          if (blockIdx.x == 0 && a.x_q_out) reinterpret_cast<uint32_t*>(a.x_q_out + (size_t)m * K)[u] = pq;
+          unsigned char* gb = xsb + (size_t)m * Kw * 16 + (u >> 2) * 16 + (u & 3);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) gb[4 * e] = (unsigned char)(pq >> (8 * e));
+          for (int e = 0; e < 4; ++e) gb[4 * e] = (unsigned char)(pq >> (8 * e));
+        }
+      }
+    } else {  // padding token: zeros in xs only
+      for (int u = tid; u < K4; u += kThreads) {
+        unsigned char* gb = xsb + (size_t)m * Kw * 16 + (u >> 2) * 16 + (u & 3);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) gb[4 * e] = 0;
+      }
     }
   }
   if (blockIdx.x == 0 && a.x_sum_out) {
@@ -303,6 +219,231 @@ __device__ __forceinline__ void fused_prologue(const StreamArgs& a, uint4* xs, f
   }
 }
 
+// Exact RMSNorm scale of one row by the whole block (taken only when the fast
+// path below cannot decide the rounding of the mean square): each warp sums its
+// squares in 128-bit fixed point relative to its own largest exponent, warp 0 brings
+// the per-warp sums to the row's largest exponent (exact unless a nonzero bit would
+// fall off, which sends the row to the exponent-bucket histogram) and forms the scale
+// with integer arithmetic only.
+__device__ __noinline__ float rms_inv_exact(const float4* xr, int K4, KDiv kd, float eps, uint32_t* red_u,
+                                            unsigned long long* red_lo, unsigned long long* red_hi,
+                                            uint32_t (*limb)[256], unsigned long long* hist, double* s_dbl,
+                                            float* s_out, int* s_flag) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t mx = 0u;
+  for (int i = tid; i < K4; i += kThreads) {
+    const float4 v = xr[i];
+    mx = max(mx, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                     max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+  }
+  const uint32_t mw = __reduce_max_sync(0xffffffffu, mx);
+  const int Ew = max((int)(mw >> 23), 1);
+  Sum128 sq;
+  sq.lo = sq.hi = 0ull;
+  bool wd = false;
+  for (int i = tid; i < K4; i += kThreads) {
+    const float4 v = xr[i];
+    sum128_add_square(sq, v.x, Ew, wd);
+    sum128_add_square(sq, v.y, Ew, wd);
+    sum128_add_square(sq, v.z, Ew, wd);
+    sum128_add_square(sq, v.w, Ew, wd);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const Sum128 t = sum128_shfl_xor(sq, o);
+    sum128_add(sq, t.lo, t.hi);
+  }
+  wd = __any_sync(0xffffffffu, wd);
+  if (lane == 0) {
+    red_lo[warp] = sq.lo;
+    red_hi[warp] = sq.hi;
+    red_u[warp] = mw | (wd ? 0x80000000u : 0u);  // bit 31: this warp's spread exceeded the window
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t t = lane < kWarps ? red_u[lane] : 0u;
+    const uint32_t w = t & 0x7fffffffu;
+    const uint32_t mb = __reduce_max_sync(0xffffffffu, w);
+    const int Eb = max((int)(mb >> 23), 1), Ewl = max((int)(w >> 23), 1);
+    Sum128 tot;
+    tot.lo = lane < kWarps ? red_lo[lane] : 0ull;
+    tot.hi = lane < kWarps ? red_hi[lane] : 0ull;
+    bool slow = (t >> 31) != 0u;
+    if (!sum128_shr_exact(tot, 2 * (Eb - Ewl))) slow = true;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {  // kWarps <= 16
+      const Sum128 u = sum128_shfl_xor(tot, o);
+      sum128_add(tot, u.lo, u.hi);
+    }
+    slow = __any_sync(0xffffffffu, slow);
+    if (lane == 0) {
+      *s_flag = slow ? 1 : 0;
+      *s_out = slow ? 0.0f : rms_inv_sum128(tot, Eb, kd, eps);
+    }
+  }
+  __syncthreads();
+  if (*s_flag) {
+    const double r = row_sumsq_hist(xr, K4, limb, hist, s_dbl);
+    if (tid == 0) *s_out = rms_inv(r, kd, eps);
+    __syncthreads();
+  }
+  const float inv = *s_out;
+  __syncthreads();  // s_out and the reduction slots may be reused by the caller
+  return inv;
+}
+
+// Quantise the activations of MT tokens (after RMSNorm when RMS) into xs
+// (byte-transposed 16-element groups); scales to s_scale.  CTA 0 also stores
+// x_q, s_x and x_sum when asked.  When xf is not NULL the first pass copies x (and
+// the gain) into shared memory, and later passes read it (with RMSNorm, the
+// normalised u replaces x there).  Barriers: one without RMSNorm; two with it in
+// the common case: the first pass also sums the squares in float-float, every warp
+// then combines the per-warp sums itself and decides the mean square when the
+// float-float accuracy suffices (else the block takes the exact path).
+template <int MT, bool RMS>
+__device__ __forceinline__ void fused_prologue(const StreamArgs& a, uint4* xs, float* xf, float* s_scale,
+                                               uint32_t* red_u, uint32_t* red_a, float2* red_ff, int* red_i,
+                                               unsigned long long* red_lo, unsigned long long* red_hi,
+                                               uint32_t (*limb)[256], unsigned long long* hist, double* s_dbl,
+                                               float* s_inv, int* s_slow) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = a.K, Kw = K >> 4, K4 = K >> 2;
+  const bool staged = xf != nullptr;
+  float4* xf4 = reinterpret_cast<float4*>(xf);  // [MT][K4] then the gain [K4]
+  const float4* g4 = staged && RMS ? xf4 + (size_t)MT * K4 : reinterpret_cast<const float4*>(a.g);
+  auto xsrc = [&](int m) -> const float4* {
+    return staged ? xf4 + (size_t)m * K4 : reinterpret_cast<const float4*>(a.x + (size_t)m * K);
+  };
+  // first pass: from global memory (staging copy), largest magnitude per token as bits
+  // and, with RMSNorm, the float-float sum of squares
+  uint32_t mx[MT];
+  FF sq[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    mx[m] = 0u;
+    // one accumulator per vector component: four independent dependency chains
+    FF s0 = {0.0f, 0.0f}, s1 = {0.0f, 0.0f}, s2 = {0.0f, 0.0f}, s3 = {0.0f, 0.0f};
+    if (m < a.M) {
+      const float4* xg = reinterpret_cast<const float4*>(a.x + (size_t)m * K);
+#pragma unroll 2
+      for (int i = tid; i < K4; i += kThreads) {
+        const float4 v = xg[i];
+        if (staged) xf4[(size_t)m * K4 + i] = v;
+        mx[m] = max(mx[m], max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                               max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+        if (RMS) {
+          ff_add_square(s0, v.x);
+          ff_add_square(s1, v.y);
+          ff_add_square(s2, v.z);
+          ff_add_square(s3, v.w);
+        }
+      }
+    }
+    if (RMS) {
+      ff_add(s0, s1);
+      ff_add(s2, s3);
+      ff_add(s0, s2);
+    }
+    sq[m] = s0;
+  }
+  if (RMS && staged) {
+    const float4* gg = reinterpret_cast<const float4*>(a.g);
+    for (int i = tid; i < K4; i += kThreads) xf4[(size_t)MT * K4 + i] = gg[i];
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    const uint32_t mw = __reduce_max_sync(0xffffffffu, mx[m]);
+    if (RMS) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        FF t;
+        t.hi = __shfl_xor_sync(0xffffffffu, sq[m].hi, o);
+        t.lo = __shfl_xor_sync(0xffffffffu, sq[m].lo, o);
+        ff_add(sq[m], t);
+      }
+    }
+    if (lane == 0) {
+      red_u[warp * MT + m] = mw;
+      if (RMS) red_ff[warp * MT + m] = make_float2(sq[m].hi, sq[m].lo);
+    }
+  }
+  __syncthreads();  // (1) per-warp maxima and sums; also publishes the staged copy
+  uint32_t am[MT];  // a = max |u| per token (u >= 0 compares as its bits)
+  if constexpr (RMS) {
+    // every warp combines the per-warp sums of each token (same values, same order:
+    // the same result in every lane of every warp) and decides the mean square
+    float inv[MT];
+    bool okm[MT];
+    bool slow = false;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      FF t;
+      t.hi = t.lo = 0.0f;
+      if (lane < kWarps) {
+        const float2 f = red_ff[lane * MT + m];
+        t.hi = f.x;
+        t.lo = f.y;
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {  // kWarps <= 16
+        FF u;
+        u.hi = __shfl_xor_sync(0xffffffffu, t.hi, o);
+        u.lo = __shfl_xor_sync(0xffffffffu, t.lo, o);
+        ff_add(t, u);
+      }
+      // lane 0's sum to every lane: the decision below (and the barriers of the exact
+      // path it may select) is then the same in every thread of the block
+      t.hi = __shfl_sync(0xffffffffu, t.hi, 0);
+      t.lo = __shfl_sync(0xffffffffu, t.lo, 0);
+      float ms = 0.0f;
+      okm[m] = m >= a.M || ff_mean_f32(t, K, a.inv_k, ms);
+      inv[m] = okm[m] ? inv_rms_f32(ms, a.eps) : 0.0f;
+      slow |= !okm[m];
+    }
+    if (slow) {  // block-uniform: every warp took the same decisions
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+        if (!okm[m])
+          inv[m] = rms_inv_exact(xsrc(m), K4, a.kd, a.eps, red_u + kWarps * MT, red_lo, red_hi, limb, hist, s_dbl,
+                                 s_inv, s_slow);
+    }
+    // second pass: u = fl(fl(x * inv) * g) (kept in the staging copy) and a = max |u|
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      am[m] = 0u;
+      if (m < a.M) {
+        const float4* xr = xsrc(m);
+#pragma unroll 2
+        for (int i = tid; i < K4; i += kThreads) {
+          const float4 v = xr[i];
+          const float4 gg = g4[i];
+          const float4 u = make_float4(__fmul_rn(__fmul_rn(v.x, inv[m]), gg.x), __fmul_rn(__fmul_rn(v.y, inv[m]), gg.y),
+                                       __fmul_rn(__fmul_rn(v.z, inv[m]), gg.z), __fmul_rn(__fmul_rn(v.w, inv[m]), gg.w));
+          if (staged) xf4[(size_t)m * K4 + i] = u;  // this thread's own slots
+          const float t = fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w)));
+          am[m] = max(am[m], __float_as_uint(t));
+        }
+      }
+      am[m] = __reduce_max_sync(0xffffffffu, am[m]);
+      if (lane == 0) red_a[warp * MT + m] = am[m];
+    }
+    __syncthreads();  // (2)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) am[m] = __reduce_max_sync(0xffffffffu, lane < kWarps ? red_a[lane * MT + m] : 0u);
+    // quantise u (from the staging copy, or recomputed from x)
+    quantise_tokens<MT>(a, xs, staged ? xf4 : nullptr, g4, inv, am, red_i, s_scale);
+  } else {
+    // without RMSNorm u = x: a is the largest |x| of the first pass
+#pragma unroll
+    for (int m = 0; m < MT; ++m) am[m] = __reduce_max_sync(0xffffffffu, lane < kWarps ? red_u[lane * MT + m] : 0u);
+    float inv[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) inv[m] = 1.0f;
+    quantise_tokens<MT>(a, xs, staged ? xf4 : reinterpret_cast<const float4*>(a.x), nullptr, inv, am, red_i,
+                        s_scale);
+  }
+}
+
 template <int MT, int JMAX, int PRE, bool FUSED, bool RMS>
 __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -313,11 +454,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
   const int row0 = c * a.rows_base + min(c, a.rows_rem);
   uint4* xs = reinterpret_cast<uint4*>(smem + a.xs_off);  // [MT][Kw] byte-transposed x_q
   int* sacc = reinterpret_cast<int*>(smem + a.acc_off);   // [nrows][MT] row totals
-  __shared__ uint32_t red_u[kWarps * MT];
+  __shared__ uint32_t red_u[kWarps * MT + (RMS ? kWarps : 0)];
+  __shared__ uint32_t red_a[RMS ? kWarps * MT : 1];
+  __shared__ float2 red_ff[RMS ? kWarps * MT : 1];
   __shared__ int red_i[kWarps * MT];
-  __shared__ unsigned long long red_lo[RMS ? kWarps * MT : 1], red_hi[RMS ? kWarps * MT : 1];
+  __shared__ unsigned long long red_lo[RMS ? kWarps : 1], red_hi[RMS ? kWarps : 1];
   __shared__ float s_scale[MT];
   __shared__ float s_inv[MT];
+  __shared__ int s_slow[1];
   __shared__ double s_dbl;
   __shared__ uint32_t limb[RMS ? 3 : 1][256];
   __shared__ unsigned long long hist[RMS ? 256 : 1];
@@ -366,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
     if (tid < MT) s_scale[tid] = tid < a.M ? a.s_x_in[tid] : 0.0f;
   } else {
     float* xf = a.xf_off >= 0 ? reinterpret_cast<float*>(smem + a.xf_off) : nullptr;
-    fused_prologue<MT, RMS>(a, xs, xf, s_scale, red_u, red_i, red_lo, red_hi, limb, hist, &s_dbl, s_inv);
+    fused_prologue<MT, RMS>(a, xs, xf, s_scale, red_u, red_a, red_ff, red_i, red_lo, red_hi, limb, hist, &s_dbl,
+                            s_inv, s_slow);
   }
   __syncthreads();
 
@@ -566,7 +711,8 @@ cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, cons
   Plan p;
   if (!make_plan(M, N, K, num_sms, p, true)) return cudaErrorInvalidValue;
   tw::StreamArgs a = {};
-  a.packed = packed; a.w_scale = w_scale; a.x = x; a.g = g; a.eps = eps;
+  a.packed = packed; a.w_scale = w_scale; a.x = x; a.g = g; a.eps = eps; a.kd = tw::make_kdiv(K);
+  a.inv_k = 1.0f / (float)K;
   a.M = M; a.N = N; a.K = K; a.y = y; a.acc_out = acc_out;
   a.x_q_out = x_q_out; a.s_x_out = s_x_out; a.x_sum_out = x_sum_out;
   fill_plan(a, p);

@@ -474,3 +474,40 @@ def test_host_pointers_rejected(tw):
                                  y.data_ptr(), None, None)
         assert st == tw.TW_ERR_NOT_DEVICE_PTR
     torch.cuda.synchronize()
+
+
+def _near_mean_square_midpoint(rng, K, scale, big):
+    """A row whose mean square lies within about 2^-35 (relative) of an fp32 rounding
+    midpoint: the fused prologue's float-float path must either decide it correctly or
+    hand it to the exact path."""
+    from fractions import Fraction
+    x = (rng.standard_normal(K) * scale).astype(np.float32)
+    if big:
+        x[-1] = np.float32(scale * 30.0)
+    rest = sum(Fraction(float(v)) ** 2 for v in x[:-1])
+    ms = np.float32(float((rest + Fraction(float(x[-1])) ** 2) / K))
+    mid = Fraction(float(ms)) + Fraction(float(np.spacing(ms))) / 2
+    need = mid * K - rest
+    if need > 0:
+        x[-1] = np.float32(float(need) ** 0.5)
+    return x
+
+
+def test_rmsnorm_mean_square_near_midpoints(tw):
+    rng = np.random.default_rng(2026)
+    K, N = 2560, 256
+    rows = [_near_mean_square_midpoint(rng, K, s, b) for s in (0.01, 1.0, 50.0) for b in (False, True)]
+    W = si.weights(N, K, seed=99)
+    p_ref, g_ref = oracle.pack_ternary(W)
+    g = si.rms_gain(K, seed=98)
+    for i in range(0, len(rows), 3):
+        x = np.stack(rows[i:i + 3])
+        ref = oracle.rmsnorm_quant_act(x, g, si.RMS_EPS)
+        got = tw.quantize(dev(x), dev(g), si.RMS_EPS)
+        for a_, b_ in zip(got, ref):
+            assert (host(a_).view(np.uint8) == b_.view(np.uint8)).all()
+        y_ref, acc_ref = oracle.ternary_matmul(p_ref, g_ref, ref[0], ref[1])
+        y, acc, xq, sx, xs, _ = fused_run(tw, x, p_ref, g_ref, g)
+        assert (xq == ref[0]).all() and (sx.view(np.uint32) == ref[1].view(np.uint32)).all()
+        assert (acc == acc_ref).all()
+        assert_y_close(y, y_ref)
