@@ -111,6 +111,12 @@ __device__ __forceinline__ float dequant(int acc, float c, float gamma, float s_
   return dequant_tiny(acc, gamma, s_x);
 }
 
+// The same for an accumulator already held exactly in fp32 (|acc| < 2^24).
+__device__ __forceinline__ float dequant_f(float acc, float c, float gamma, float s_x) {
+  if (__builtin_expect(c >= 1.17549435e-38f, 1)) return __fmul_rn(acc, c);
+  return dequant_tiny(__float2int_rn(acc), gamma, s_x);
+}
+
 // ---------------------------------------------------------------------------
 // Exact sum of squares of an fp32 row, fast path.
 //

@@ -770,103 +770,95 @@ constexpr int TB_STAGE = TBN * BK * 2;         // 32 KB of widened weights per s
 constexpr int TA_STAGE = 128 * BK * 2;         // 16 KB of activations per stage
 constexpr int TW_RAW = TBN * (BK / 4);         // 4 KB of packed codes per stage
 constexpr int kTokNA = 6, kTokNB = 3, kTokARing = 4;
-constexpr int kPartStride = TBN + 4;           // floats per token row of the split-K partials
+constexpr int kPartStride = TBN + 4;           // floats per token row of the staged partials
 constexpr int kTokThreads = 320;               // warps 0-7 convert + epilogue, 8: TMA, 9: MMA
 
 __device__ __forceinline__ void pdl_wait_all() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Epilogue of the tokens-on-M kernel.  Warp w reads tensor-memory lanes 32 (w % 4)
-// .. +31 (its tokens) and the weight-row half w / 4.  With a K split the partial
-// sums go to this CTA's shared memory as [token][kPartStride] and CTA crank of the
-// cluster finishes rows [crank * 256/ksplit, ...) for every real token, reading
-// four consecutive rows at a time from every rank and storing them as one float4.
+// .. +31 (its tokens) and the weight-row half w / 4, 32 columns at a time, and
+// stages them in its own CTA's shared memory as part[token][row] (rows padded to
+// 260 floats: conflict-free for one token per lane).  The 256 rows of the tile are
+// finished by the ksplit CTAs of the cluster, W = 256 / ksplit each: after a cluster
+// barrier every CTA reads its rows of every rank's partials, four consecutive rows of
+// a token per thread (each warp reads and stores 512 contiguous bytes), adds them in
+// fp32 (the partial sums are integers below 2^24 in magnitude, so every sum is
+// exact) and stores them dequantised as one float4; a second barrier keeps every CTA
+// until its peers are done reading.  The flags of all ranks are read before the
+// second barrier.
 __device__ __forceinline__ void tok_epilogue(const Args& a, uint32_t tmem, float* part, volatile int* abort_flag,
                                              int any_fail, int nk, int n0, uint32_t crank, const float* scale) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, half = warp >> 2;
   const int m = quarter * 32 + lane;  // token of this thread
+  const int ks = a.ksplit, W = TBN / ks;
   const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
   const float gam = __ldg(a.w_scale);
   const bool vec = (a.N & 3) == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(a.acc_out) & 15) == 0;  // 16-byte stores allowed
-  const bool warp_live = quarter * 32 < a.M;  // some token of this warp is real (warp-uniform)
-  int cluster_fail = any_fail;
-  // outputs n .. n+3 of token mm
-  auto store4 = [&](int mm, int n, int a0, int a1, int a2, int a3) {
-    const float sm = scale[mm], c = scale[128 + mm];
-    float* yrow = a.y + (size_t)mm * a.N;
-    if (vec && n + 4 <= a.N) {
-      *reinterpret_cast<float4*>(yrow + n) =
-          make_float4(dequant(a0, c, gam, sm), dequant(a1, c, gam, sm), dequant(a2, c, gam, sm), dequant(a3, c, gam, sm));
-      if (a.acc_out) *reinterpret_cast<int4*>(a.acc_out + (size_t)mm * a.N + n) = make_int4(a0, a1, a2, a3);
-    } else {
-      const int av[4] = {a0, a1, a2, a3};
-      for (int q = 0; q < 4; ++q) {
-        if (n + q < a.N) {
-          yrow[n + q] = dequant(av[q], c, gam, sm);
-          if (a.acc_out) a.acc_out[(size_t)mm * a.N + n + q] = av[q];
-        }
-      }
-    }
-  };
-  if (a.ksplit > 1) {
-    if (warp < 8 && warp_live && !any_fail) {
-      for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
-        uint32_t v[32];
-        if (nk > 0) {
-          tmem_ld32(taddr + (uint32_t)c0, v);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = 0u;
-        }
-        float4* dst = reinterpret_cast<float4*>(part + (size_t)m * kPartStride + c0);
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-          dst[t] = make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]), __uint_as_float(v[4 * t + 2]),
-                               __uint_as_float(v[4 * t + 3]));
-      }
-    }
-    if (tid == 0) *abort_flag = any_fail;
-    cluster_sync();
-    for (int rk = 0; rk < a.ksplit; ++rk)
-      cluster_fail |= *static_cast<volatile int*>(__cluster_map_shared_rank((void*)abort_flag, (unsigned)rk));
-    if (!cluster_fail) {
-      const int per4 = TBN / a.ksplit / 4;  // groups of 4 rows finished by this CTA
-      const int r0 = (int)crank * (TBN / a.ksplit);
-      const float* src[kMaxCluster];
-#pragma unroll
-      for (int rk = 0; rk < kMaxCluster; ++rk)
-        src[rk] = static_cast<const float*>(__cluster_map_shared_rank((void*)part, (unsigned)(rk < a.ksplit ? rk : 0)));
-      for (int it = tid; it < a.M * per4; it += kTokThreads) {
-        const int mm = it / per4, c = r0 + 4 * (it % per4);
-        float4 v[kMaxCluster];
-#pragma unroll
-        for (int rk = 0; rk < kMaxCluster; ++rk)
-          v[rk] = rk < a.ksplit ? *reinterpret_cast<const float4*>(src[rk] + (size_t)mm * kPartStride + c)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        int acc[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int rk = 0; rk < kMaxCluster; ++rk) {
-          acc[0] += __float2int_rn(v[rk].x); acc[1] += __float2int_rn(v[rk].y);
-          acc[2] += __float2int_rn(v[rk].z); acc[3] += __float2int_rn(v[rk].w);
-        }
-        store4(mm, n0 + c, acc[0], acc[1], acc[2], acc[3]);
-      }
-    }
-    cluster_sync();  // no CTA leaves while others still read its shared memory
-  } else if (warp < 8 && warp_live && !any_fail) {
+  if (warp < 8 && quarter * 32 < a.M && !any_fail) {
     for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
       uint32_t v[32];
-      tmem_ld32(taddr + (uint32_t)c0, v);
-      if (m < a.M) {
+      if (nk > 0) {
+        tmem_ld32(taddr + (uint32_t)c0, v);
+      } else {
 #pragma unroll
-        for (int t = 0; t < 32; t += 4)
-          store4(m, n0 + c0 + t, __float2int_rn(__uint_as_float(v[t])), __float2int_rn(__uint_as_float(v[t + 1])),
-                 __float2int_rn(__uint_as_float(v[t + 2])), __float2int_rn(__uint_as_float(v[t + 3])));
+        for (int t = 0; t < 32; ++t) v[t] = 0u;
+      }
+      uint4* dst = reinterpret_cast<uint4*>(part + (size_t)m * kPartStride + c0);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) dst[t] = make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+    }
+  }
+  if (tid == 0) *abort_flag = any_fail;
+  if (ks > 1) cluster_sync();
+  else __syncthreads();
+  int cluster_fail = any_fail;
+  if (ks > 1) {
+    for (int rk = 0; rk < ks; ++rk)
+      cluster_fail |= *static_cast<volatile int*>(__cluster_map_shared_rank((void*)abort_flag, (unsigned)rk));
+  }
+  if (!cluster_fail) {
+    const int per4 = W / 4;
+    const int r0 = (int)crank * W;
+    const float* src[kMaxCluster];
+#pragma unroll
+    for (int rk = 0; rk < kMaxCluster; ++rk)
+      src[rk] = ks > 1 ? static_cast<const float*>(__cluster_map_shared_rank((void*)part, (unsigned)(rk < ks ? rk : 0)))
+                       : part;
+    for (int it = tid; it < a.M * per4; it += kTokThreads) {
+      const int mm = it / per4, c = r0 + 4 * (it % per4);
+      float4 acc = *reinterpret_cast<const float4*>(src[0] + (size_t)mm * kPartStride + c);
+#pragma unroll
+      for (int rk = 1; rk < kMaxCluster; ++rk) {
+        if (rk < ks) {
+          const float4 f = *reinterpret_cast<const float4*>(src[rk] + (size_t)mm * kPartStride + c);
+          acc.x = __fadd_rn(acc.x, f.x); acc.y = __fadd_rn(acc.y, f.y);
+          acc.z = __fadd_rn(acc.z, f.z); acc.w = __fadd_rn(acc.w, f.w);
+        }
+      }
+      const int n = n0 + c;
+      const float sm = scale[mm], cs = scale[128 + mm];
+      float* yrow = a.y + (size_t)mm * a.N;
+      if (vec && n + 4 <= a.N) {
+        *reinterpret_cast<float4*>(yrow + n) = make_float4(dequant_f(acc.x, cs, gam, sm), dequant_f(acc.y, cs, gam, sm),
+                                                           dequant_f(acc.z, cs, gam, sm), dequant_f(acc.w, cs, gam, sm));
+        if (a.acc_out)
+          *reinterpret_cast<int4*>(a.acc_out + (size_t)mm * a.N + n) =
+              make_int4(__float2int_rn(acc.x), __float2int_rn(acc.y), __float2int_rn(acc.z), __float2int_rn(acc.w));
+      } else {
+        const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+        for (int q = 0; q < 4; ++q) {
+          if (n + q < a.N) {
+            yrow[n + q] = dequant_f(av[q], cs, gam, sm);
+            if (a.acc_out) a.acc_out[(size_t)mm * a.N + n + q] = __float2int_rn(av[q]);
+          }
+        }
       }
     }
   }
+  if (ks > 1) cluster_sync();  // no CTA leaves while others still read its shared memory
   if (tid == 0 && cluster_fail) atomicExch(&g_gemm_status, (int)TW_ERR_TIMEOUT);
 }
 
@@ -1179,7 +1171,7 @@ bool gemm_tok_plan(int M, int N, int K, int num_sms, GemmPlan& p) {
   p.nstages = kTokNA;
   size_t body = (size_t)kTokNA * TA_STAGE + (size_t)kTokNB * TB_STAGE + (size_t)kTokARing * TW_RAW;
   const size_t partial = (size_t)128 * kPartStride * 4;
-  if (p.ksplit > 1 && body < partial) body = partial;
+  if (body < partial) body = partial;
   p.ctrl_off = (uint32_t)body;
   p.smem = 1024 + body + kCtrlBytes;
   if (p.smem < 114 * 1024) p.smem = 114 * 1024;
