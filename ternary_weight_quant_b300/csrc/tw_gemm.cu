@@ -275,23 +275,24 @@ __device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* pa
         float4 v[kMaxCluster];  // every rank's partials in flight together
 #pragma unroll
         for (int rk = 0; rk < kMaxCluster; ++rk) v[rk] = rk < a.ksplit ? src[rk][e] : make_float4(0.f, 0.f, 0.f, 0.f);
-        int4 acc = make_int4(0, 0, 0, 0);
+        // integers below 2^24 in magnitude: the fp32 sums are exact
+        float4 acc = v[0];
 #pragma unroll
-        for (int rk = 0; rk < kMaxCluster; ++rk) {
-          acc.x += __float2int_rn(v[rk].x); acc.y += __float2int_rn(v[rk].y);
-          acc.z += __float2int_rn(v[rk].z); acc.w += __float2int_rn(v[rk].w);
+        for (int rk = 1; rk < kMaxCluster; ++rk) {
+          acc.x = __fadd_rn(acc.x, v[rk].x); acc.y = __fadd_rn(acc.y, v[rk].y);
+          acc.z = __fadd_rn(acc.z, v[rk].z); acc.w = __fadd_rn(acc.w, v[rk].w);
         }
         const int j = t0 + (4 * e) / BM, rr = (4 * e) % BM;
         const int m = m0 + j;
         if (m < a.M) {
           const float sm = sxs[j], c = cs[j];
-          const int av[4] = {acc.x, acc.y, acc.z, acc.w};
+          const float av[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const int n = n0 + rr + t;
             if (n < a.N) {
-              a.y[(size_t)m * a.N + n] = dequant(av[t], c, gam, sm);
-              if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = av[t];
+              a.y[(size_t)m * a.N + n] = dequant_f(av[t], c, gam, sm);
+              if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = __float2int_rn(av[t]);
             }
           }
         }
@@ -309,9 +310,9 @@ __device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* pa
         for (int t = 0; t < 32; ++t) {
           const int j = c0 + t, m = m0 + j;
           if (m < a.M && nv) {
-            const int acc = __float2int_rn(__uint_as_float(v[t]));
-            a.y[(size_t)m * a.N + n] = dequant(acc, cs[j], gam, sxs[j]);
-            if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = acc;
+            const float acc = __uint_as_float(v[t]);
+            a.y[(size_t)m * a.N + n] = dequant_f(acc, cs[j], gam, sxs[j]);
+            if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = __float2int_rn(acc);
           }
         }
       }
@@ -323,9 +324,9 @@ __device__ __forceinline__ void epilogue(const Args& a, uint32_t tmem, float* pa
         for (int t = 0; t < 8; ++t) {
           const int j = c0 + t, m = m0 + j;
           if (m < a.M && nv) {
-            const int acc = __float2int_rn(__uint_as_float(v[t]));
-            a.y[(size_t)m * a.N + n] = dequant(acc, cs[j], gam, sxs[j]);
-            if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = acc;
+            const float acc = __uint_as_float(v[t]);
+            a.y[(size_t)m * a.N + n] = dequant_f(acc, cs[j], gam, sxs[j]);
+            if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = __float2int_rn(acc);
           }
         }
       }
