@@ -193,13 +193,14 @@ TW_API tw_status tw_ternary_gemv(const uint8_t *packed, const float *w_scale, co
  *   acc_out  [M][N] int32 accumulators, or NULL.
  * Requires 1 <= M <= TW_QUANT_GEMV_MAX_M, N >= 1, K % 64 == 0, 64 <= K <= TW_MAX_K;
  * TW_ERR_UNSUPPORTED when the shape does not fit the kernel's shared memory.
- * Launched with programmatic dependent launch: the kernel starts streaming
- * `packed` into shared memory before the previous kernel on `stream` has
- * finished, and reads x (and writes every output) only after it has.  So the
- * packed weights must not be written by the kernel enqueued immediately before
- * this call on `stream` (weights packed at load time, with any later
- * synchronisation or any other kernel in between, are fine).  The same holds for
- * w_scale, which is also read before that point.
+ * Launched with programmatic dependent launch: the kernel starts loading
+ * `packed` into registers before the previous kernel on `stream` has finished,
+ * and reads x (and writes every output) only after it has (x is only prefetched
+ * into the coherent L2 before that point).  So the packed weights must not be
+ * written by the kernel enqueued immediately before this call on `stream`
+ * (weights packed at load time, with any later synchronisation or any other
+ * kernel in between, are fine).  The same holds for w_scale and the RMSNorm gain
+ * g, which are also read before that point.
  */
 TW_API tw_status tw_quant_gemv(const float *x, const float *g, float eps, const uint8_t *packed,
                                const float *w_scale, int64_t M, int64_t N, int64_t K, float *y,

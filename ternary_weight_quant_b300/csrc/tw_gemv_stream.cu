@@ -294,8 +294,8 @@ __device__ __noinline__ float rms_inv_exact(const float4* xr, int K4, KDiv kd, f
 
 // Quantise the activations of MT tokens (after RMSNorm when RMS) into xs
 // (byte-transposed 16-element groups); scales to s_scale.  CTA 0 also stores
-// x_q, s_x and x_sum when asked.  When xf is not NULL the first pass copies x (and
-// the gain) into shared memory, and later passes read it (with RMSNorm, the
+// x_q, s_x and x_sum when asked.  When xf is not NULL the first pass copies x into
+// shared memory (the gain is already there), and later passes read it (with RMSNorm, the
 // normalised u replaces x there).  Barriers: one without RMSNorm; two with it in
 // the common case: the first pass also sums the squares in float-float, every warp
 // then combines the per-warp sums itself and decides the mean square when the
@@ -346,10 +346,7 @@ __device__ __forceinline__ void fused_prologue(const StreamArgs& a, uint4* xs, f
     }
     sq[m] = s0;
   }
-  if (RMS && staged) {
-    const float4* gg = reinterpret_cast<const float4*>(a.g);
-    for (int i = tid; i < K4; i += kThreads) xf4[(size_t)MT * K4 + i] = gg[i];
-  }
+  // (with RMSNorm and staging, the gain was staged before the dependency wait)
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     const uint32_t mw = __reduce_max_sync(0xffffffffu, mx[m]);
@@ -495,6 +492,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
   const float gam = __ldg(a.w_scale);
 
   for (int i = tid; i < nrows * MT; i += kThreads) sacc[i] = 0;
+  if constexpr (FUSED) {
+    // The RMSNorm gain, like the weights, is a parameter: stage it now.  x may come from
+    // the previous kernel, so it is only prefetched into L2 (coherent; no data is read
+    // into the SM before the wait).
+    if (RMS && a.xf_off >= 0) {
+      float4* gst = reinterpret_cast<float4*>(smem + a.xf_off) + (size_t)MT * (K >> 2);
+      const float4* gg = reinterpret_cast<const float4*>(a.g);
+      for (int i = tid; i < (K >> 2); i += kThreads) gst[i] = __ldg(gg + i);
+    }
+    for (int i = tid; i < a.M * (K >> 5); i += kThreads)  // one 128-byte line per thread
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.x + (size_t)i * 32) : "memory");
+    if (RMS && a.xf_off < 0) {
+      for (int i = tid; i < (K >> 5); i += kThreads) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.g + (size_t)i * 32) : "memory");
+    }
+  }
   pdl_wait();  // activations and outputs may belong to the previous kernel
 
   // ---------------------------------------------------------------- activations -> xs
