@@ -583,13 +583,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
   __syncthreads();
 
   // ---------------------------------------------------------------- epilogue (coalesced)
-  for (int i = tid; i < a.M * nrows; i += kThreads) {
-    const int m = i / nrows, r = i - m * nrows;
-    const int acc = sacc[r * MT + m];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    if (m >= a.M) break;
     const float sm = s_scale[m];
-    const size_t o = (size_t)m * a.N + row0 + r;
-    a.y[o] = dequant(acc, dequant_scale(gam, sm), gam, sm);
-    if (a.acc_out) a.acc_out[o] = acc;
+    const float c = dequant_scale(gam, sm);  // once per token, not per output
+    for (int r = tid; r < nrows; r += kThreads) {
+      const int acc = sacc[r * MT + m];
+      const size_t o = (size_t)m * a.N + row0 + r;
+      a.y[o] = dequant(acc, c, gam, sm);
+      if (a.acc_out) a.acc_out[o] = acc;
+    }
   }
 }
 
