@@ -26,6 +26,10 @@ roofline: the product kernel.  Average launch duration = the timed region's devi
           copy rate (or bf16 tensor rate).  traffic = DRAM bytes per launch from the committed
           ncu summary when it was taken on the unchanged kernel, else null.
 cpu_baseline / --impl reference: the CPU oracle (oracle/), as it stands, on the host.
+Default workload only, as extra keys: us_per_layer_unfused (the same step with the
+quantisations as separate kernels), small_case (K = N = 256, M = 1: microseconds per
+call, latency-bound) and read_stream (a read-only streaming rate, the third bandwidth
+basis next to the nominal 8 TB/s and the measured copy rate).
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling,
 no data-path collective); rank 0 prints max-over-ranks time and the summed bytes.
@@ -437,6 +441,50 @@ def timed_replays(graph, steps, world):
     return start.elapsed_time(stop) / 1e3
 
 
+def small_case_latency(tw, reps: int = 200):
+    """K = N = 256, M = 1 (the small configuration): fused quantisation + GEMV, `reps` calls
+    chained in one CUDA graph; latency-bound, so reported as microseconds per call."""
+    import torch
+    import seeded_inputs as si
+    W = si.device_normal((256, 256), seed=0)
+    packed, gamma = tw.pack(W)
+    x = si.device_normal((1, 256), seed=1)
+    y = torch.empty((1, 256), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tw.tw_quant_gemv(x, packed, gamma, y)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            tw.tw_quant_gemv(x, packed, gamma, y)
+    for _ in range(3):
+        g.replay()
+    el = timed_replays(g, 5, 1)
+    return {"shape": "256x256, M = 1, fused quantisation", "us_per_call": el / (5 * reps) * 1e6,
+            "calls_per_graph": reps}
+
+
+def read_stream_rate(gib: float = 2.0):
+    """A read-only streaming rate (torch.amax over a 2 GiB fp32 buffer, CUDA events): a
+    third bandwidth basis next to the nominal figure and the measured copy rate."""
+    import torch
+    buf = torch.ones(int(gib * (1 << 30)) // 4, dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        torch.amax(buf)
+    a, b = events_new(), events_new()
+    a.record()
+    for _ in range(5):
+        torch.amax(buf)
+    b.record()
+    torch.cuda.synchronize()
+    gbs = 5 * buf.numel() * 4 / (a.elapsed_time(b) / 1e3) / 1e9
+    del buf
+    return {"GB/s": gbs, "how": "torch.amax over a 2 GiB fp32 buffer, 5 passes"}
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -542,6 +590,20 @@ def run_ours(args):
     e2e_el, e2e_bytes = combine_over_ranks(e0.elapsed_time(e1) / 1e3, bytes_per_step * e2e_steps, world)
     e2e_value = e2e_bytes / e2e_el / 1e9
 
+    # ---- default workload only: the unfused variant of the same step, the smallest case's
+    # latency per call, and a read-only streaming rate as a third bandwidth basis
+    extra = {}
+    if args.workload == "2b" and not args.separate:
+        ugraph = capture(stack, fused=False)
+        for _ in range(args.warmup):
+            ugraph.replay()
+        u_el = timed_replays(ugraph, args.steps, world)
+        extra["us_per_layer_unfused"] = u_el / args.steps / layers * 1e6
+        extra["launches_per_step_unfused"] = stack.launches_per_step(False)
+        del ugraph
+        extra["small_case"] = small_case_latency(tw)
+        extra["read_stream"] = read_stream_rate()
+
     # ---- CPU baseline: the oracle on the host, bounded sample (rank 0, N = 1, default workload)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "2b":
@@ -578,6 +640,9 @@ def run_ours(args):
             "TFLOP/s": ops_per_step * args.steps * world / elapsed_max / 1e12,
             "pct_of_nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
             "pct_of_measured_copy": 100.0 * value / world / peak_hbm,
+            **({"pct_of_measured_read": 100.0 * value / world / extra["read_stream"]["GB/s"]}
+               if "read_stream" in extra else {}),
+            **extra,
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak,
                          "traffic": recorded_traffic(args.workload) if fused else None,
