@@ -495,7 +495,10 @@ def run_ours(args):
     import ternary_weight_quant_b300 as tw
 
     model, layers, M, distinct = WORKLOADS[args.workload]
-    fused = (not args.separate) and M <= 4
+    # one token: quantisation fused into the GEMV launch; 2-4 tokens: separate kernels, which
+    # measured faster (70B at 4 tokens: 241.6 against 275.4 us per layer; the fused prologue
+    # quantises its tokens one after another)
+    fused = (not args.separate) and M == 1
     stack = DecodeStack(tw, layers, M=M, model=model, distinct=distinct)
     plan = layer_plan(model)
     bytes_per_step = step_bytes(M, model, layers)
@@ -666,17 +669,17 @@ def run_ours(args):
 
 
 def run_kernel_case(args):
-    """One kernel in isolation (for timing sweeps and small ncu captures; not the contract line).
+    """Kernels in isolation (for timing sweeps and small ncu captures; not the contract line).
 
-    --kernel-case {gemv,fused,fused_rms,quant,rms_quant,gemm} on --shape NxK at --M tokens, over
-    --copies distinct weight tensors (so the stream leaves L2); one pass over them is captured in
-    a CUDA graph and replayed --reps times (device time per launch, host launch cost excluded)."""
+    --kernel-case {gemv,fused,fused_rms,quant,rms_quant,gemm,gemm_nows} (a comma list) on --shape
+    NxK at --M tokens (a comma list), over --copies distinct weight tensors (so the stream leaves
+    L2); one pass over them is captured in a CUDA graph and replayed --reps times (device time
+    per launch, host launch cost excluded).  One JSON line per (case, M)."""
     import torch
     import seeded_inputs as si
     torch.cuda.set_device(0)
     import ternary_weight_quant_b300 as tw
     N, K = (int(v) for v in args.shape.lower().split("x"))
-    M = args.M
     ws = torch.empty(tw.tw_pack_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
     packs = []
     for c in range(args.copies):
@@ -686,55 +689,62 @@ def run_kernel_case(args):
         tw.tw_pack_ternary(W, p, g, ws)
         del W
         packs.append((p, g))
-    x = si.device_normal((M, K), seed=5)
     gain = 1.0 + 0.1 * si.device_normal((K,), seed=6)
-    xq, sx, xs = tw.quantize(x)
-    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    gws = tw.gemm_workspace(M, K)
-    k = args.kernel_case
+    for M in (int(v) for v in str(args.M).split(",")):
+        x = si.device_normal((M, K), seed=5)
+        xq, sx, xs = tw.quantize(x)
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        gws = tw.gemm_workspace(M, K)
+        for k in args.kernel_case.split(","):
 
-    def launch(p, g):
-        if k == "gemv":
-            tw.tw_ternary_gemv(p, g, xq, sx, y, xs)
-        elif k in ("fused", "fused_rms"):
-            tw.tw_quant_gemv(x, p, g, y, g=gain if k == "fused_rms" else None)
-        elif k == "quant":
-            tw.tw_quant_act(x, xq, sx, xs)
-        elif k == "rms_quant":
-            tw.tw_rmsnorm_quant_act(x, gain, 1e-6, xq, sx, xs)
-        elif k == "gemm":
-            tw.tw_ternary_gemm(p, g, xq, sx, y, workspace=gws)
-        elif k == "gemm_nows":
-            tw.tw_ternary_gemm(p, g, xq, sx, y)
-        else:
-            raise SystemExit(f"unknown kernel case {k}")
+            def launch(p, g):
+                if k == "gemv":
+                    tw.tw_ternary_gemv(p, g, xq, sx, y, xs)
+                elif k in ("fused", "fused_rms"):
+                    tw.tw_quant_gemv(x, p, g, y, g=gain if k == "fused_rms" else None)
+                elif k == "quant":
+                    tw.tw_quant_act(x, xq, sx, xs)
+                elif k == "rms_quant":
+                    tw.tw_rmsnorm_quant_act(x, gain, 1e-6, xq, sx, xs)
+                elif k == "gemm":
+                    tw.tw_ternary_gemm(p, g, xq, sx, y, workspace=gws)
+                elif k == "gemm_nows":
+                    tw.tw_ternary_gemm(p, g, xq, sx, y)
+                else:
+                    raise SystemExit(f"unknown kernel case {k}")
 
-    def one_pass():
-        for p, g in packs:
-            launch(p, g)
+            def one_pass():
+                for p, g in packs:
+                    launch(p, g)
 
-    # one pass over the copies captured in a CUDA graph, so host launch cost does not show
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        one_pass()  # warm-up (and lazy initialisation) outside the capture
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        one_pass()
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    a, b = events_new(), events_new()
-    a.record()
-    for _ in range(args.reps):
-        graph.replay()
-    b.record()
-    torch.cuda.synchronize()
-    us = a.elapsed_time(b) * 1e3 / (args.reps * len(packs))
-    print(json.dumps({"kernel_case": k, "N": N, "K": K, "M": M, "us_per_launch": us,
-                      "GB/s": gemv_bytes(N, K, M) / us / 1e3, "TFLOP/s": 2 * M * N * K / us / 1e6}))
+            try:
+                # one pass over the copies captured in a CUDA graph, so host launch cost does not show
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(s):
+                    one_pass()  # warm-up (and lazy initialisation) outside the capture
+                torch.cuda.current_stream().wait_stream(s)
+                torch.cuda.synchronize()
+            except tw.TWError as e:
+                print(json.dumps({"kernel_case": k, "N": N, "K": K, "M": M, "unsupported": str(e)}))
+                continue
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                one_pass()
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+            a, b = events_new(), events_new()
+            a.record()
+            for _ in range(args.reps):
+                graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / (args.reps * len(packs))
+            print(json.dumps({"kernel_case": k, "N": N, "K": K, "M": M, "us_per_launch": us,
+                              "GB/s": gemv_bytes(N, K, M) / us / 1e3, "TFLOP/s": 2 * M * N * K / us / 1e6}),
+                  flush=True)
+            del graph
     return 0
 
 
@@ -752,7 +762,7 @@ def main():
     ap.add_argument("--kernel-case", default=None,
                     help="time one kernel alone: gemv, fused, fused_rms, quant, rms_quant, gemm or gemm_nows")
     ap.add_argument("--shape", default="13824x2560", help="NxK for --kernel-case")
-    ap.add_argument("--M", type=int, default=1, help="tokens for --kernel-case")
+    ap.add_argument("--M", default="1", help="tokens for --kernel-case (a comma list)")
     ap.add_argument("--copies", type=int, default=8, help="distinct weight tensors for --kernel-case")
     ap.add_argument("--reps", type=int, default=3, help="passes over the copies for --kernel-case")
     args = ap.parse_args()

@@ -239,7 +239,8 @@ TW_API tw_status tw_ternary_gemm(const uint8_t *packed, const float *w_scale, co
                                  size_t ws_bytes, tw_stream_t stream);
 
 /*
- * The product for any M: tw_ternary_gemv below the measured crossover (M <= 16),
+ * The product for any M: tw_ternary_gemv below the measured crossover (M <= 16; M <= 11
+ * for matrices of 2^24 weights or more when a large enough workspace is given, K % 64 == 0),
  * tw_ternary_gemm above it (when K % 16 == 0 and packed / x_q are 16-byte aligned; an
  * exact CUDA-core kernel otherwise).  Arguments as tw_ternary_gemm; the workspace is
  * used only on the tensor-core path and may be NULL.

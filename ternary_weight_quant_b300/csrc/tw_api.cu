@@ -264,8 +264,20 @@ TW_API tw_status tw_ternary_gemm(const uint8_t* packed, const float* w_scale, co
   return from_cuda(e);
 }
 
-// Token count from which the tensor-core GEMM takes over from the GEMV kernels.
+// Token count from which the tensor-core GEMM takes over from the GEMV kernels.  Between 9
+// and 16 tokens the dp4a GEMV's cost grows with M while the tokens-on-M GEMM's stays flat, so
+// for large matrices (N K >= 2^24, e.g. 13824 x 2560 or 2560 x 6912) the GEMM takes over at 12
+// tokens when it can use its workspace (measured on B300: at 12 tokens 2560 x 6912 takes
+// 21.1 us as a GEMV and 14.6 us as a GEMM; 3840 x 2560 stays faster as a GEMV up to 16).
 static const int64_t kGemmCrossoverM = 17;
+static const int64_t kGemmCrossoverLargeM = 12;
+static const int64_t kLargeWeights = (int64_t)1 << 24;
+
+static bool prefer_gemm(int64_t M, int64_t N, int64_t K, const void* workspace, size_t ws_bytes) {
+  if (M >= kGemmCrossoverM || M > TW_GEMV_MAX_M) return true;
+  return M >= kGemmCrossoverLargeM && N * K >= kLargeWeights && K % 64 == 0 && workspace != nullptr &&
+         ws_bytes >= tw_gemm_ws_size((int)M, (int)K);
+}
 
 TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
                                    const float* s_x, const int32_t* x_sum, int64_t M, int64_t N, int64_t K,
@@ -273,7 +285,7 @@ TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, 
                                    tw_stream_t stream) {
   tw_status st = check_product_args(packed, w_scale, x_q, s_x, M, N, K, y);
   if (st != TW_OK) return st;
-  if (M < kGemmCrossoverM && M <= TW_GEMV_MAX_M)
+  if (!prefer_gemm(M, N, K, workspace, ws_bytes))
     return tw_ternary_gemv(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, stream);
   if (K % 16 == 0 && aligned(x_q, 16) && aligned(packed, 16))
     return tw_ternary_gemm(packed, w_scale, x_q, s_x, x_sum, M, N, K, y, acc_out, workspace, ws_bytes, stream);

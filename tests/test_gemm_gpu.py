@@ -139,3 +139,13 @@ def test_matmul_dispatch_parity(tw, M):
     packed, gamma, xq, sx, y_ref, acc_ref = case(M, 384, 2560, seed=M)
     y, acc = run_gemm(tw, packed, gamma, xq, sx, fn="tw_ternary_matmul")
     check(y, acc, y_ref, acc_ref)
+
+
+@pytest.mark.parametrize("ws", [True, False])
+@pytest.mark.parametrize("M", [11, 12, 16])
+def test_matmul_large_matrix_crossover(tw, M, ws):
+    """For matrices of 2^24 weights or more (here 2560 x 6912) the dispatch hands 12..16 tokens
+    to the GEMM when a workspace is given, and keeps the GEMV otherwise: the same exact result."""
+    packed, gamma, xq, sx, y_ref, acc_ref = case(M, 2560, 6912, seed=300 + M)
+    y, acc = run_gemm(tw, packed, gamma, xq, sx, fn="tw_ternary_matmul", ws=ws)
+    check(y, acc, y_ref, acc_ref)
