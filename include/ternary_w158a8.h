@@ -229,9 +229,13 @@ TW_API size_t tw_gemm_workspace_bytes(int64_t M, int64_t K);
  *              layout; without it every CTA widens its own activation tiles (slower).
  *              Its contents on entry do not matter; it must not be used by other work
  *              until this call's work on `stream` has finished.
- * Tiles of 128 weight rows x up to 256 tokens; K is split over a thread-block cluster
- * (up to 8 CTAs, partial sums combined through distributed shared memory) when the
- * tile grid alone would leave SMs idle.
+ * Tiles: up to 128 tokens (with the workspace) x 256 weight rows, the tokens on the
+ * MMA's M side; otherwise 128 weight rows x up to 256 tokens.  K is split over a
+ * thread-block cluster (up to 8 CTAs, partial sums combined through distributed shared
+ * memory) when the tile grid alone would leave SMs idle.  With the workspace the GEMM
+ * kernel is launched with programmatic dependent launch behind the widening kernel (its
+ * weight fetches overlap that kernel; everything enqueued before this call has
+ * finished by then, so no extra condition applies to the caller).
  */
 TW_API tw_status tw_ternary_gemm(const uint8_t *packed, const float *w_scale, const int8_t *x_q,
                                  const float *s_x, const int32_t *x_sum, int64_t M, int64_t N,
