@@ -9,154 +9,236 @@
 //             ms = (float)(r / K) (the double division emulated with integers),
 //             inv = 1 / sqrt(ms + eps) (IEEE fp32 sqrt and divide),
 //             u = fl(fl(x * inv) * g);
+//             ms is first decided from a float-float sum of squares when its error
+//             bound leaves the rounding determined; the exact path above otherwise;
 //   a = max |u|;  x_q = clamp(rne(fl(fl(u * 127) / a)), -128, 127);  s_x = a;
 //   x_sum = sum x_q.
-// All fp32 steps use the _rn intrinsics, so no contraction or approximate
-// division changes a rounding.
+// All fp32 steps use the _rn intrinsics, so no contraction changes a rounding; the
+// approximate steps (the float-float mean square, the approximate reciprocal of the
+// quantisation) are used only where their error bound leaves the result decided, and
+// the exact operation is taken otherwise.
 #include "tw_common.cuh"
 
 namespace tw {
 
+// Exact RMSNorm scale of row xr by the whole block (rare path: the float-float mean
+// square could not be decided).  The row's largest exponent E comes from mx (its
+// largest magnitude's bits); 128-bit fixed point relative to E, or the exponent-bucket
+// histogram when the exponents spread further.
+__device__ __noinline__ float act_rms_inv_exact(const float4* xr, int K4, uint32_t mx, KDiv kd, float eps,
+                                                uint32_t (*limb)[256], unsigned long long* hist,
+                                                unsigned long long* red_lo, unsigned long long* red_hi,
+                                                float* sh_inv) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int E = max((int)(mx >> 23), 1);
+  Sum128 sq;
+  sq.lo = sq.hi = 0ull;
+  bool wide = false;
+  for (int i = tid; i < K4; i += blockDim.x) {
+    const float4 v = xr[i];
+    sum128_add_square(sq, v.x, E, wide);
+    sum128_add_square(sq, v.y, E, wide);
+    sum128_add_square(sq, v.z, E, wide);
+    sum128_add_square(sq, v.w, E, wide);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const Sum128 t = sum128_shfl_xor(sq, o);
+    sum128_add(sq, t.lo, t.hi);
+  }
+  const int any_wide = __syncthreads_or(wide ? 1 : 0);
+  if (lane == 0) {
+    red_lo[warp] = sq.lo;
+    red_hi[warp] = sq.hi;
+  }
+  __syncthreads();
+  if (!any_wide) {
+    if (tid == 0) {
+      Sum128 t;
+      t.lo = t.hi = 0ull;
+      for (int w = 0; w < nwarps; ++w) sum128_add(t, red_lo[w], red_hi[w]);
+      *sh_inv = rms_inv_sum128(t, E, kd, eps);
+    }
+  } else {
+    for (int i = tid; i < 256; i += blockDim.x) limb[0][i] = limb[1][i] = limb[2][i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < K4; i += blockDim.x) {
+      const float4 v = xr[i];
+      const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t mm;
+        int b;
+        f32_bucket(e[j], mm, b);
+        if (mm) {
+          const unsigned long long q = (unsigned long long)mm * mm;
+          atomicAdd(&limb[0][b], (uint32_t)(q & 0xffffu));
+          atomicAdd(&limb[1][b], (uint32_t)((q >> 16) & 0xffffu));
+          atomicAdd(&limb[2][b], (uint32_t)(q >> 32));
+        }
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < 256; i += blockDim.x)
+      hist[i] = (unsigned long long)limb[0][i] + ((unsigned long long)limb[1][i] << 16) +
+                ((unsigned long long)limb[2][i] << 32);
+    __syncthreads();
+    if (warp == 0) {
+      const double r = warp_exact_hist_to_double(hist, 256, 2, -298);
+      if (lane == 0) *sh_inv = rms_inv(r, kd, eps);
+    }
+  }
+  __syncthreads();
+  const float inv = *sh_inv;
+  __syncthreads();
+  return inv;
+}
+
+// One CTA per token.  First pass: max |x| and (RMSNorm) the float-float sum of squares;
+// every warp then combines the per-warp values itself and decides the mean square when
+// the float-float accuracy suffices (the exact path otherwise); second pass (RMSNorm):
+// a = max |u|; last pass: quantise (conversion-free rounding, the IEEE divide only for a
+// unit with a quotient near a half-integer), store, sum.
 template <bool RMS>
 __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict__ x,
                                                         const float* __restrict__ g, float eps, int K, KDiv kd,
-                                                        int8_t* __restrict__ x_q, float* __restrict__ s_x,
-                                                        int32_t* __restrict__ x_sum) {
+                                                        float inv_k, int8_t* __restrict__ x_q,
+                                                        float* __restrict__ s_x, int32_t* __restrict__ x_sum) {
   const int m = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int K4 = K >> 2;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)m * K);
   const float4* g4 = reinterpret_cast<const float4*>(g);
-  // exact sum of squares: per exponent bucket, m^2 (< 2^48) split into three 16-bit
-  // limbs summed with native 32-bit shared atomics (K <= 65532 keeps each < 2^32)
   __shared__ uint32_t limb[RMS ? 3 : 1][RMS ? 256 : 1];
   __shared__ unsigned long long hist[RMS ? 256 : 1];
-  __shared__ float red_f[32];
   __shared__ int red_i[32];
-  __shared__ uint32_t red_u[32];
+  __shared__ uint32_t red_u[32], red_a[32];
+  __shared__ float2 red_ff[32];
   __shared__ unsigned long long red_lo[32], red_hi[32];
-  __shared__ float sh_inv, sh_amax;
+  __shared__ float sh_inv;
 
-  float inv = 1.0f;
+  // first pass
+  uint32_t mx = 0u;
+  FF s0 = {0.0f, 0.0f}, s1 = {0.0f, 0.0f}, s2 = {0.0f, 0.0f}, s3 = {0.0f, 0.0f};
+#pragma unroll 2
+  for (int i = tid; i < K4; i += blockDim.x) {
+    const float4 v = xr[i];
+    mx = max(mx, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                     max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+    if (RMS) {
+      ff_add_square(s0, v.x);
+      ff_add_square(s1, v.y);
+      ff_add_square(s2, v.z);
+      ff_add_square(s3, v.w);
+    }
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
   if (RMS) {
-    // E = largest biased exponent of the row (from the largest magnitude's bits)
-    uint32_t mx = 0u;
-    for (int i = tid; i < K4; i += blockDim.x) {
-      const float4 v = xr[i];
-      mx = max(mx, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
-                       max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
-    }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0) red_u[warp] = mx;
-    __syncthreads();
-    mx = 0u;
-    for (int w = 0; w < nwarps; ++w) mx = max(mx, red_u[w]);
-    const int E = max((int)(mx >> 23), 1);
-    // exact sum of squares in 128-bit fixed point (fast path)
-    Sum128 sq;
-    sq.lo = sq.hi = 0ull;
-    bool wide = false;
-    for (int i = tid; i < K4; i += blockDim.x) {
-      const float4 v = xr[i];
-      sum128_add_square(sq, v.x, E, wide);
-      sum128_add_square(sq, v.y, E, wide);
-      sum128_add_square(sq, v.z, E, wide);
-      sum128_add_square(sq, v.w, E, wide);
-    }
+    ff_add(s0, s1);
+    ff_add(s2, s3);
+    ff_add(s0, s2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const Sum128 t = sum128_shfl_xor(sq, o);
-      sum128_add(sq, t.lo, t.hi);
+      FF t;
+      t.hi = __shfl_xor_sync(0xffffffffu, s0.hi, o);
+      t.lo = __shfl_xor_sync(0xffffffffu, s0.lo, o);
+      ff_add(s0, t);
     }
-    const int any_wide = __syncthreads_or(wide ? 1 : 0);
-    if (lane == 0) {
-      red_lo[warp] = sq.lo;
-      red_hi[warp] = sq.hi;
+  }
+  if (lane == 0) {
+    red_u[warp] = mx;
+    if (RMS) red_ff[warp] = make_float2(s0.hi, s0.lo);
+  }
+  __syncthreads();  // (1)
+  mx = __reduce_max_sync(0xffffffffu, lane < nwarps ? red_u[lane] : 0u);
+
+  float inv = 1.0f;
+  uint32_t am = mx;  // without RMSNorm a = max |x|
+  if constexpr (RMS) {
+    FF t;
+    t.hi = t.lo = 0.0f;
+    if (lane < nwarps) {
+      const float2 f = red_ff[lane];
+      t.hi = f.x;
+      t.lo = f.y;
     }
-    __syncthreads();
-    if (!any_wide) {
-      if (tid == 0) {
-        Sum128 t;
-        t.lo = t.hi = 0ull;
-        for (int w = 0; w < nwarps; ++w) sum128_add(t, red_lo[w], red_hi[w]);
-        sh_inv = rms_inv_sum128(t, E, kd, eps);
-      }
-    } else {
-      // exponents spread too far for 128 bits: exact exponent-bucket histogram
-      for (int i = tid; i < 256; i += blockDim.x) limb[0][i] = limb[1][i] = limb[2][i] = 0u;
-      __syncthreads();
-      for (int i = tid; i < K4; i += blockDim.x) {
-        const float4 v = xr[i];
-        const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t mm;
-          int b;
-          f32_bucket(e[j], mm, b);
-          if (mm) {
-            const unsigned long long q = (unsigned long long)mm * mm;
-            atomicAdd(&limb[0][b], (uint32_t)(q & 0xffffu));
-            atomicAdd(&limb[1][b], (uint32_t)((q >> 16) & 0xffffu));
-            atomicAdd(&limb[2][b], (uint32_t)(q >> 32));
-          }
-        }
-      }
-      __syncthreads();
-      for (int i = tid; i < 256; i += blockDim.x)
-        hist[i] = (unsigned long long)limb[0][i] + ((unsigned long long)limb[1][i] << 16) +
-                  ((unsigned long long)limb[2][i] << 32);
-      __syncthreads();
-      if (warp == 0) {
-        const double r = warp_exact_hist_to_double(hist, 256, 2, -298);
-        if (lane == 0) sh_inv = rms_inv(r, kd, eps);
-      }
+    for (int o = 8; o > 0; o >>= 1) {  // nwarps <= 16
+      FF u;
+      u.hi = __shfl_xor_sync(0xffffffffu, t.hi, o);
+      u.lo = __shfl_xor_sync(0xffffffffu, t.lo, o);
+      ff_add(t, u);
     }
-    __syncthreads();
-    inv = sh_inv;
+    // lane 0's sum to every lane: the decision is the same in every thread of the block
+    t.hi = __shfl_sync(0xffffffffu, t.hi, 0);
+    t.lo = __shfl_sync(0xffffffffu, t.lo, 0);
+    float ms = 0.0f;
+    if (ff_mean_f32(t, K, inv_k, ms)) {
+      inv = inv_rms_f32(ms, eps);
+    } else {  // block-uniform
+      inv = act_rms_inv_exact(xr, K4, mx, kd, eps, limb, hist, red_lo, red_hi, &sh_inv);
+    }
+    // second pass: a = max |u|
+    am = 0u;
+#pragma unroll 2
+    for (int i = tid; i < K4; i += blockDim.x) {
+      const float4 v = xr[i];
+      const float4 gg = g4[i];
+      const float4 u = make_float4(__fmul_rn(__fmul_rn(v.x, inv), gg.x), __fmul_rn(__fmul_rn(v.y, inv), gg.y),
+                                   __fmul_rn(__fmul_rn(v.z, inv), gg.z), __fmul_rn(__fmul_rn(v.w, inv), gg.w));
+      am = max(am, __float_as_uint(fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w)))));
+    }
+    am = __reduce_max_sync(0xffffffffu, am);
+    if (lane == 0) red_a[warp] = am;
+    __syncthreads();  // (2)
+    am = __reduce_max_sync(0xffffffffu, lane < nwarps ? red_a[lane] : 0u);
   }
 
-  auto norm = [&](float v, float gg) -> float { return RMS ? __fmul_rn(__fmul_rn(v, inv), gg) : v; };
-
-  // pass: a = max |u|
-  float a = 0.0f;
-  for (int i = tid; i < K4; i += blockDim.x) {
-    const float4 v = xr[i];
-    float4 gg = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (RMS) gg = g4[i];
-    a = fmaxf(a, fabsf(norm(v.x, gg.x)));
-    a = fmaxf(a, fabsf(norm(v.y, gg.y)));
-    a = fmaxf(a, fabsf(norm(v.z, gg.z)));
-    a = fmaxf(a, fabsf(norm(v.w, gg.w)));
-  }
-  a = warp_max(a);
-  if (lane == 0) red_f[warp] = a;
-  __syncthreads();
-  if (warp == 0) {
-    float t = lane < nwarps ? red_f[lane] : 0.0f;
-    t = warp_max(t);
-    if (lane == 0) sh_amax = t;
-  }
-  __syncthreads();
-  a = sh_amax;
-
-  // pass: quantise, store, sum
-  const float ra = a > 0.0f ? __frcp_rn(a) : 0.0f;
+  // last pass: quantise, store, sum.  d = fl(p ra) with ra within one ulp of 1 / a
+  // (rcp.approx) is within |p/a| 2^-22 < 3.1e-5 of p / a (|p/a| <= 127) and fl32(p/a)
+  // within 2^-18 of it: at least 5e-5 from a half-integer, rint(d) is the rounding of
+  // fl32(p / a); units with an element nearer (or a non-finite d: ra is NaN when a lies
+  // outside [2^-120, 2^120]) are redone with the IEEE divide.
+  const float a = __uint_as_float(am);
+  float ra = a == 0.0f ? 0.0f : __int_as_float(0x7fffffff);
+  if (a >= 0x1p-120f && a <= 0x1p120f) asm("rcp.approx.f32 %0, %1;" : "=f"(ra) : "f"(a));
   int sum = 0;
-  char4* out = reinterpret_cast<char4*>(x_q + (size_t)m * K);
-  for (int i = tid; i < K4; i += blockDim.x) {
-    const float4 v = xr[i];
-    float4 gg = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (RMS) gg = g4[i];
-    const float u[4] = {norm(v.x, gg.x), norm(v.y, gg.y), norm(v.z, gg.z), norm(v.w, gg.w)};
-    int q[4];
+  uint32_t* out = reinterpret_cast<uint32_t*>(x_q + (size_t)m * K);
+  for (int base = warp * 32; base < K4; base += blockDim.x) {  // warp-uniform trip count
+    const int i = base + lane;
+    float uu[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t pq = 0u;
+    bool near = false;
+    if (i < K4) {
+      const float4 v = xr[i];
+      float4 gg = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (RMS) gg = g4[i];
+      uu[0] = RMS ? __fmul_rn(__fmul_rn(v.x, inv), gg.x) : v.x;
+      uu[1] = RMS ? __fmul_rn(__fmul_rn(v.y, inv), gg.y) : v.y;
+      uu[2] = RMS ? __fmul_rn(__fmul_rn(v.z, inv), gg.z) : v.z;
+      uu[3] = RMS ? __fmul_rn(__fmul_rn(v.w, inv), gg.w) : v.w;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      int t = 0;
-      if (a > 0.0f) t = quant_div(__fmul_rn(u[j], 127.0f), a, ra);
-      q[j] = max(-128, min(127, t));
-      sum += q[j];
+      for (int j = 0; j < 4; ++j) {
+        const float d = __fmul_rn(__fmul_rn(uu[j], 127.0f), ra);
+        const float sb = __fadd_rn(d, 12582912.0f);  // d + 1.5 2^23: rounds d to an integer
+        near |= !(fabsf(__fsub_rn(d, __fsub_rn(sb, 12582912.0f))) < 0.49995f);
+        const int t = (int)(__float_as_uint(sb) & 0x7fffffu) - 0x400000;
+        pq |= ((uint32_t)max(-128, min(127, t)) & 0xffu) << (8 * j);
+      }
     }
-    out[i] = make_char4((signed char)q[0], (signed char)q[1], (signed char)q[2], (signed char)q[3]);
+    if (__any_sync(0xffffffffu, near) && near) {  // rare
+      pq = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int t = a > 0.0f ? __float2int_rn(__fdiv_rn(__fmul_rn(uu[j], 127.0f), a)) : 0;
+        pq |= ((uint32_t)max(-128, min(127, t)) & 0xffu) << (8 * j);
+      }
+    }
+    if (i < K4) {
+      out[i] = pq;
+      sum += (int)(int8_t)(pq & 0xffu) + (int)(int8_t)((pq >> 8) & 0xffu) + (int)(int8_t)((pq >> 16) & 0xffu) +
+             (int)(int8_t)(pq >> 24);
+    }
   }
   sum = warp_sum(sum);
   if (lane == 0) red_i[warp] = sum;
@@ -182,13 +264,13 @@ static int act_threads(long long K) {
 
 cudaError_t tw_launch_quant_act(const float* x, long long M, long long K, int8_t* x_q, float* s_x,
                                 int32_t* x_sum, cudaStream_t stream) {
-  tw::act_quant_kernel<false><<<(unsigned)M, act_threads(K), 0, stream>>>(x, nullptr, 0.0f, (int)K, tw::make_kdiv((int)K), x_q, s_x,
+  tw::act_quant_kernel<false><<<(unsigned)M, act_threads(K), 0, stream>>>(x, nullptr, 0.0f, (int)K, tw::make_kdiv((int)K), 1.0f / (float)K, x_q, s_x,
                                                                          x_sum);
   return cudaGetLastError();
 }
 
 cudaError_t tw_launch_rmsnorm_quant_act(const float* x, const float* g, float eps, long long M, long long K,
                                         int8_t* x_q, float* s_x, int32_t* x_sum, cudaStream_t stream) {
-  tw::act_quant_kernel<true><<<(unsigned)M, act_threads(K), 0, stream>>>(x, g, eps, (int)K, tw::make_kdiv((int)K), x_q, s_x, x_sum);
+  tw::act_quant_kernel<true><<<(unsigned)M, act_threads(K), 0, stream>>>(x, g, eps, (int)K, tw::make_kdiv((int)K), 1.0f / (float)K, x_q, s_x, x_sum);
   return cudaGetLastError();
 }
