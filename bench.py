@@ -224,6 +224,20 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+def host_cpu() -> str:
+    """The host CPU model and its logical core count, for the CPU-baseline description."""
+    model = "unknown CPU"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return f"{model}, {os.cpu_count()} logical cores on the host"
+
+
 def oracle_layer_sample(layer_data, seconds_min: float, seconds_max: float):
     """Run the oracle's decode-layer sequence over host copies of layers until >= seconds_min.
 
@@ -287,7 +301,8 @@ def run_reference(args):
             "data": "synthetic",
             "config": {"workload": WORKLOAD + "; oracle step = one layer (bounded sample)", "M": 1},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "one 2B-shaped layer per step (RMSNorm/quant + 4 GEMVs), single thread"},
+                             "sample": "one 2B-shaped layer per step (RMSNorm/quant + 4 GEMVs), single thread; "
+                                       + host_cpu()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -614,7 +629,7 @@ def run_ours(args):
         b, el, n = oracle_layer_sample(olayers, args.cpu_seconds, 3 * args.cpu_seconds)
         cpu = {"value": b / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} run(s) of one 2B-shaped layer (RMSNorm/quant + 4 GEMVs, M=1), "
-                         f"single thread, {el:.1f} s"}
+                         f"single thread, {el:.1f} s; {host_cpu()}"}
 
     if rank == 0:
         if fused:
