@@ -140,3 +140,17 @@ def test_alignment_checks(tw):
     assert lib.tw_ternary_gemv(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 16, FAKE + 2, None, None) == tw.TW_ERR_ALIGN
     assert lib.tw_ternary_gemm(FAKE, FAKE, FAKE + 4, FAKE, None, 64, 4, 16, FAKE, None, None, 0,
                                None) == tw.TW_ERR_ALIGN
+
+
+def test_import_fails_loudly_without_the_library(tmp_path):
+    """A copy of the package without libtw.so must refuse to import: there is no CPU path."""
+    import shutil
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = tmp_path / "ternary_weight_quant_b300"
+    pkg.mkdir()
+    shutil.copy(os.path.join(root, "ternary_weight_quant_b300", "__init__.py"), pkg / "__init__.py")
+    r = subprocess.run([sys.executable, "-c", "import ternary_weight_quant_b300"], cwd=str(tmp_path),
+                       capture_output=True, text=True, env={**os.environ, "PYTHONPATH": str(tmp_path)})
+    assert r.returncode != 0 and "libtw.so not built" in r.stderr
