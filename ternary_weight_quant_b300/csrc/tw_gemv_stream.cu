@@ -91,12 +91,14 @@ __device__ __forceinline__ void breduce_sum_i32(int (&v)[MT], int* red) {
 
 // Exact sum of squares of one row by the whole block through the exponent-bucket
 // histogram (slow path for rows with a wide exponent spread).
+template <int NW>
 __device__ double row_sumsq_hist(const float4* xr, int K4, uint32_t (*limb)[256], unsigned long long* hist,
                                  double* out) {
+  constexpr int NT = NW * 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < 256; i += kThreads) limb[0][i] = limb[1][i] = limb[2][i] = 0u;
+  for (int i = tid; i < 256; i += NT) limb[0][i] = limb[1][i] = limb[2][i] = 0u;
   __syncthreads();
-  for (int i = tid; i < K4; i += kThreads) {
+  for (int i = tid; i < K4; i += NT) {
     const float4 v = xr[i];
     const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -113,7 +115,7 @@ __device__ double row_sumsq_hist(const float4* xr, int K4, uint32_t (*limb)[256]
     }
   }
   __syncthreads();
-  for (int i = tid; i < 256; i += kThreads)
+  for (int i = tid; i < 256; i += NT)
     hist[i] = (unsigned long long)limb[0][i] + ((unsigned long long)limb[1][i] << 16) +
               ((unsigned long long)limb[2][i] << 32);
   __syncthreads();
@@ -225,13 +227,16 @@ __device__ __forceinline__ void quantise_tokens(const StreamArgs& a, uint4* xs, 
 // the per-warp sums to the row's largest exponent (exact unless a nonzero bit would
 // fall off, which sends the row to the exponent-bucket histogram) and forms the scale
 // with integer arithmetic only.
+template <int NW>
 __device__ __noinline__ float rms_inv_exact(const float4* xr, int K4, KDiv kd, float eps, uint32_t* red_u,
                                             unsigned long long* red_lo, unsigned long long* red_hi,
                                             uint32_t (*limb)[256], unsigned long long* hist, double* s_dbl,
                                             float* s_out, int* s_flag) {
+  static_assert(NW <= 16, "the cross-warp combine below covers at most 16 warps");
+  constexpr int NT = NW * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t mx = 0u;
-  for (int i = tid; i < K4; i += kThreads) {
+  for (int i = tid; i < K4; i += NT) {
     const float4 v = xr[i];
     mx = max(mx, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
                      max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
@@ -241,7 +246,7 @@ __device__ __noinline__ float rms_inv_exact(const float4* xr, int K4, KDiv kd, f
   Sum128 sq;
   sq.lo = sq.hi = 0ull;
   bool wd = false;
-  for (int i = tid; i < K4; i += kThreads) {
+  for (int i = tid; i < K4; i += NT) {
     const float4 v = xr[i];
     sum128_add_square(sq, v.x, Ew, wd);
     sum128_add_square(sq, v.y, Ew, wd);
@@ -261,17 +266,17 @@ __device__ __noinline__ float rms_inv_exact(const float4* xr, int K4, KDiv kd, f
   }
   __syncthreads();
   if (warp == 0) {
-    const uint32_t t = lane < kWarps ? red_u[lane] : 0u;
+    const uint32_t t = lane < NW ? red_u[lane] : 0u;
     const uint32_t w = t & 0x7fffffffu;
     const uint32_t mb = __reduce_max_sync(0xffffffffu, w);
     const int Eb = max((int)(mb >> 23), 1), Ewl = max((int)(w >> 23), 1);
     Sum128 tot;
-    tot.lo = lane < kWarps ? red_lo[lane] : 0ull;
-    tot.hi = lane < kWarps ? red_hi[lane] : 0ull;
+    tot.lo = lane < NW ? red_lo[lane] : 0ull;
+    tot.hi = lane < NW ? red_hi[lane] : 0ull;
     bool slow = (t >> 31) != 0u;
     if (!sum128_shr_exact(tot, 2 * (Eb - Ewl))) slow = true;
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {  // kWarps <= 16
+    for (int o = 8; o > 0; o >>= 1) {  // NW <= 16
       const Sum128 u = sum128_shfl_xor(tot, o);
       sum128_add(tot, u.lo, u.hi);
     }
@@ -283,7 +288,7 @@ __device__ __noinline__ float rms_inv_exact(const float4* xr, int K4, KDiv kd, f
   }
   __syncthreads();
   if (*s_flag) {
-    const double r = row_sumsq_hist(xr, K4, limb, hist, s_dbl);
+    const double r = row_sumsq_hist<NW>(xr, K4, limb, hist, s_dbl);
     if (tid == 0) *s_out = rms_inv(r, kd, eps);
     __syncthreads();
   }
@@ -401,7 +406,7 @@ __device__ __forceinline__ void fused_prologue(const StreamArgs& a, uint4* xs, f
 #pragma unroll
       for (int m = 0; m < MT; ++m)
         if (!okm[m])
-          inv[m] = rms_inv_exact(xsrc(m), K4, a.kd, a.eps, red_u + kWarps * MT, red_lo, red_hi, limb, hist, s_dbl,
+          inv[m] = rms_inv_exact<kWarps>(xsrc(m), K4, a.kd, a.eps, red_u + kWarps * MT, red_lo, red_hi, limb, hist, s_dbl,
                                  s_inv, s_slow);
     }
     // second pass: u = fl(fl(x * inv) * g) (kept in the staging copy) and a = max |u|
@@ -597,6 +602,451 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
   }
 }
 
+// ---------------------------------------------------------------------------
+// One token (the decode step): the whole weight block of a CTA copied to shared memory
+// before the dependency wait, a lean fused prologue, and per-warp row outputs.
+//
+// * Before griddepcontrol.wait one thread starts bulk copies (cp.async.bulk, completion on
+//   an mbarrier) of the CTA's rows -- contiguous in the packed tensor -- into shared
+//   memory: the weight stream of this GEMV runs while the previous kernel finishes,
+//   without holding registers.  Everything else that does not depend on the previous
+//   kernel (the RMSNorm gain, the row mapping) is also prepared before the wait.
+// * After the wait every thread loads its part of x (all loads in flight at once: one L2
+//   round trip) and stages it in shared memory.
+// * Pass 1 (registers only): per warp either the largest |x| (no RMSNorm: that is a) or,
+//   with RMSNorm, the float-float sum of squares and the float4 holding the largest
+//   p = fl(|x| |g|).  After the first barrier every warp combines the per-warp results
+//   itself (same values, same order: the same result in every warp).  With RMSNorm the
+//   scale a = max_k |u_k|, u_k = fl(fl(x_k inv) g_k), is first taken over that float4:
+//   both roundings are relative errors of at most 2^-24 for normal results, so only an
+//   element whose p lies within a few units of 2^-24 of the largest one can have a
+//   larger |u|.  The quantisation pass checks |u_k| <= a for every element it quantises
+//   anyway; when some element exceeds it (near-ties, underflow) the block takes the
+//   maximum over all elements and quantises once more.  Two block barriers in the
+//   common case, whatever RMSNorm, and the result is always exact.
+// * Dot products from shared memory, up to four rows at a time (independent chains,
+//   no padded rows computed); a warp that owns whole rows writes their outputs itself.
+constexpr int kDecWarps = 16;
+constexpr int kDecThreads = kDecWarps * 32;
+
+struct DecodeRed {
+  float2 ff[kDecWarps];   // per-warp float-float sums of squares
+  uint32_t pm[kDecWarps]; // per-warp largest p (RMSNorm) or |x|, as bits
+  int pi[kDecWarps];      // float4 index of that p
+  uint32_t am[kDecWarps]; // re-check: per-warp largest |u|
+  int qs[kDecWarps];      // per-warp sums of x_q (CTA 0, when asked)
+  int viol;               // some |u_k| exceeded the candidate scale
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool dec_mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase (2 s of wall time).
+__device__ __forceinline__ bool dec_mbar_wait(uint32_t bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (dec_mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > 2000000000ull) return false;
+    }
+  }
+}
+
+// Quantises this thread's NV float4s of x (registers: xv, and the gain gv when RMS) with
+// scale amax into xs; float4 q of the thread is unit tid + q * kDecThreads.  Returns the
+// thread's sum of x_q; sets *viol when `check` and some |u| > amax.
+template <bool RMS, int NV>
+__device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, const float4 (&xv)[NV],
+                                               const float4 (&gv)[NV], float inv, float amax, bool check,
+                                               int* viol) {
+  const int tid = threadIdx.x;
+  const int K4 = a.K >> 2;
+  unsigned char* xsb = reinterpret_cast<unsigned char*>(xs);
+  float ra = amax == 0.0f ? 0.0f : __int_as_float(0x7fffffff);
+  if (amax >= 0x1p-120f && amax <= 0x1p120f) asm("rcp.approx.f32 %0, %1;" : "=f"(ra) : "f"(amax));
+  // d = fl(fl(u 127) ra) is within 2^-22 |d| < 3.1e-5 of fl(u 127) / a (|d| <= 127 once
+  // |u| <= a); when it is at least 5e-5 from a half-integer, rounding d gives
+  // round_half_even(fl32(fl(u 127) / a)).  Rounding by adding 1.5 2^23: the integer is then
+  // in the low mantissa bits, its two's-complement low byte in the low byte of the sum.
+  // Units with an element nearer a half-integer (or a non-finite d) take the IEEE divide.
+  uint32_t pq[NV];
+  bool near[NV];
+  bool any = false, bad = false;
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    const bool valid = tid + q * kDecThreads < K4;
+    float4 v = valid ? xv[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (RMS) {
+      const float4 gg = gv[q];
+      v = make_float4(__fmul_rn(__fmul_rn(v.x, inv), gg.x), __fmul_rn(__fmul_rn(v.y, inv), gg.y),
+                      __fmul_rn(__fmul_rn(v.z, inv), gg.z), __fmul_rn(__fmul_rn(v.w, inv), gg.w));
+      if (check && valid) bad |= fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) > amax;
+    }
+    const float d0 = __fmul_rn(__fmul_rn(v.x, 127.0f), ra), d1 = __fmul_rn(__fmul_rn(v.y, 127.0f), ra);
+    const float d2 = __fmul_rn(__fmul_rn(v.z, 127.0f), ra), d3 = __fmul_rn(__fmul_rn(v.w, 127.0f), ra);
+    const float s0 = __fadd_rn(d0, 12582912.0f), s1 = __fadd_rn(d1, 12582912.0f);
+    const float s2 = __fadd_rn(d2, 12582912.0f), s3 = __fadd_rn(d3, 12582912.0f);
+    const float e = fmaxf(fmaxf(fabsf(__fsub_rn(d0, __fsub_rn(s0, 12582912.0f))),
+                                fabsf(__fsub_rn(d1, __fsub_rn(s1, 12582912.0f)))),
+                          fmaxf(fabsf(__fsub_rn(d2, __fsub_rn(s2, 12582912.0f))),
+                                fabsf(__fsub_rn(d3, __fsub_rn(s3, 12582912.0f)))));
+    near[q] = valid && !(e < 0.49995f);  // also when some d is not finite
+    any |= near[q];
+    pq[q] = __byte_perm(__byte_perm(__float_as_uint(s0), __float_as_uint(s1), 0x0040u),
+                        __byte_perm(__float_as_uint(s2), __float_as_uint(s3), 0x0040u), 0x5410u);
+  }
+  if (__any_sync(0xffffffffu, any) && any) {  // rare: the IEEE divide for units near a tie
+    auto q_exact = [&](float uv) -> uint32_t {
+      const int t = amax > 0.0f ? __float2int_rn(__fdiv_rn(__fmul_rn(uv, 127.0f), amax)) : 0;
+      return (uint32_t)max(-128, min(127, t)) & 0xffu;
+    };
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      if (near[q]) {
+        float4 v = xv[q];
+        if (RMS) {
+          const float4 gg = gv[q];
+          v = make_float4(__fmul_rn(__fmul_rn(v.x, inv), gg.x), __fmul_rn(__fmul_rn(v.y, inv), gg.y),
+                          __fmul_rn(__fmul_rn(v.z, inv), gg.z), __fmul_rn(__fmul_rn(v.w, inv), gg.w));
+        }
+        pq[q] = q_exact(v.x) | (q_exact(v.y) << 8) | (q_exact(v.z) << 16) | (q_exact(v.w) << 24);
+      }
+    }
+  }
+  int qsum = 0;
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    const int u = tid + q * kDecThreads;
+    if (u < K4) {
+      qsum = __dp4a((int)pq[q], 0x01010101, qsum);
+      if (blockIdx.x == 0 && a.x_q_out) reinterpret_cast<uint32_t*>(a.x_q_out)[u] = pq[q];
+      // element k of 16-element group k/16 goes to byte (k/4) % 4 of word k % 4
+      unsigned char* gb = xsb + (u >> 2) * 16 + (u & 3);
+      gb[0] = (unsigned char)pq[q];
+      gb[4] = (unsigned char)(pq[q] >> 8);
+      gb[8] = (unsigned char)(pq[q] >> 16);
+      gb[12] = (unsigned char)(pq[q] >> 24);
+    }
+  }
+  if (bad) *viol = 1;
+  return qsum;
+}
+
+// The one-token prologue: x (fp32, global) -> xs (byte-transposed int8 groups).  Returns
+// a = max |u|; sets *cs to the dequantisation scale fl(fl(gamma a) / 127) and *xtot to the
+// sum of x_q over the whole row.  A thread holds float4s tid + q * kDecThreads (q < NV,
+// NV * kDecThreads >= K/4) of x, and of the gain in gv (RMS; loaded before the dependency
+// wait).  xf4 is the staging area for x ([K/4] float4), followed by the staged gain.
+template <bool RMS, int NV>
+__device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs, float4* xf4, const float4 (&gv)[NV],
+                                                 DecodeRed& r, uint32_t* red_u, unsigned long long* red_lo,
+                                                 unsigned long long* red_hi, uint32_t (*limb)[256],
+                                                 unsigned long long* hist, double* s_dbl, float* s_inv,
+                                                 int* s_slow, float gam, float* cs, int* xtot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned full = 0xffffffffu;
+  const int K = a.K, K4 = K >> 2;
+  const float4* g4 = xf4 + K4;
+  const float4* xg = reinterpret_cast<const float4*>(a.x);
+
+  // ---- x: this thread's loads all in flight, then staged for the other warps
+  float4 xv[NV];
+#pragma unroll
+  for (int q = 0; q < NV; ++q)
+    xv[q] = tid + q * kDecThreads < K4 ? __ldcg(xg + tid + q * kDecThreads) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < NV; ++q)
+    if (tid + q * kDecThreads < K4) xf4[tid + q * kDecThreads] = xv[q];
+
+  // ---- pass 1 (padding float4s are zero: they add nothing)
+  FF s0 = {0.0f, 0.0f}, s1 = {0.0f, 0.0f}, s2 = {0.0f, 0.0f}, s3 = {0.0f, 0.0f};
+  float pmf = 0.0f;
+  int pi = 0;
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    const float4 v = xv[q];
+    if (RMS) {
+      const float4 gg = gv[q];
+      ff_add_square(s0, v.x);  // one chain per component
+      ff_add_square(s1, v.y);
+      ff_add_square(s2, v.z);
+      ff_add_square(s3, v.w);
+      const float m = fmaxf(fmaxf(fabsf(__fmul_rn(v.x, gg.x)), fabsf(__fmul_rn(v.y, gg.y))),
+                            fmaxf(fabsf(__fmul_rn(v.z, gg.z)), fabsf(__fmul_rn(v.w, gg.w))));
+      if (m > pmf) {
+        pmf = m;
+        pi = tid + q * kDecThreads;
+      }
+    } else {
+      pmf = fmaxf(pmf, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+  }
+  const uint32_t pm = __float_as_uint(pmf);  // >= 0: compares as its bits
+  const uint32_t wm = __reduce_max_sync(full, pm);
+  if (RMS) {
+    ff_add(s0, s1);
+    ff_add(s2, s3);
+    ff_add(s0, s2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      FF t;
+      t.hi = __shfl_xor_sync(full, s0.hi, o);
+      t.lo = __shfl_xor_sync(full, s0.lo, o);
+      ff_add(s0, t);
+    }
+    const int wi = __shfl_sync(full, pi, __ffs(__ballot_sync(full, pm == wm)) - 1);
+    if (lane == 0) {
+      r.ff[warp] = make_float2(s0.hi, s0.lo);
+      r.pi[warp] = wi;
+    }
+  }
+  if (lane == 0) r.pm[warp] = wm;
+  if (tid == 0) r.viol = 0;
+  __syncthreads();  // (1) per-warp results and the staged copy of x
+
+  // ---- every warp: combine (kDecWarps <= 16 partials, one per lane)
+  const uint32_t ml = lane < kDecWarps ? r.pm[lane] : 0u;
+  const uint32_t bm = __reduce_max_sync(full, ml);
+  float amax, inv = 1.0f;
+  if constexpr (!RMS) {
+    amax = __uint_as_float(bm);
+  } else {
+    FF t;
+    t.hi = t.lo = 0.0f;
+    if (lane < kDecWarps) {
+      const float2 f = r.ff[lane];
+      t.hi = f.x;
+      t.lo = f.y;
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      FF u;
+      u.hi = __shfl_xor_sync(full, t.hi, o);
+      u.lo = __shfl_xor_sync(full, t.lo, o);
+      ff_add(t, u);
+    }
+    t.hi = __shfl_sync(full, t.hi, 0);  // the same decision in every thread of the block
+    t.lo = __shfl_sync(full, t.lo, 0);
+    float ms = 0.0f;
+    if (ff_mean_f32(t, K, a.inv_k, ms)) {
+      inv = inv_rms_f32(ms, a.eps);
+    } else {  // block-uniform
+      inv = rms_inv_exact<kDecWarps>(xf4, K4, a.kd, a.eps, red_u, red_lo, red_hi, limb, hist, s_dbl, s_inv, s_slow);
+    }
+    const int pil = lane < kDecWarps ? r.pi[lane] : 0;
+    const int ks = __shfl_sync(full, pil, __ffs(__ballot_sync(full, lane < kDecWarps && ml == bm)) - 1);
+    const float4 v = xf4[ks], gg = g4[ks];
+    amax = fmaxf(fmaxf(fabsf(__fmul_rn(__fmul_rn(v.x, inv), gg.x)), fabsf(__fmul_rn(__fmul_rn(v.y, inv), gg.y))),
+                 fmaxf(fabsf(__fmul_rn(__fmul_rn(v.z, inv), gg.z)), fabsf(__fmul_rn(__fmul_rn(v.w, inv), gg.w))));
+  }
+  *cs = dequant_scale(gam, amax);
+
+  // ---- quantisation (with RMSNorm: checks the candidate scale)
+  int qsum = decode_quantise<RMS, NV>(a, xs, xv, gv, inv, amax, RMS, &r.viol);
+  qsum = __reduce_add_sync(full, qsum);
+  if (lane == 0) r.qs[warp] = qsum;
+  __syncthreads();  // (2) xs and the per-warp sums complete; r.viol final
+  if (RMS && r.viol) {  // block-uniform, rare: a from all elements, then quantise again
+    float m = 0.0f;
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      const float4 v = xv[q], gg = gv[q];
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(__fmul_rn(__fmul_rn(v.x, inv), gg.x)), fabsf(__fmul_rn(__fmul_rn(v.y, inv), gg.y))),
+                         fmaxf(fabsf(__fmul_rn(__fmul_rn(v.z, inv), gg.z)), fabsf(__fmul_rn(__fmul_rn(v.w, inv), gg.w)))));
+    }
+    const uint32_t am = __reduce_max_sync(full, __float_as_uint(m));
+    if (lane == 0) r.am[warp] = am;
+    __syncthreads();
+    amax = __uint_as_float(__reduce_max_sync(full, lane < kDecWarps ? r.am[lane] : 0u));
+    *cs = dequant_scale(gam, amax);
+    qsum = decode_quantise<RMS, NV>(a, xs, xv, gv, inv, amax, false, &r.viol);
+    qsum = __reduce_add_sync(full, qsum);
+    __syncthreads();  // every warp has read r.am and r.qs
+    if (lane == 0) r.qs[warp] = qsum;
+    __syncthreads();
+  }
+  *xtot = __reduce_add_sync(full, lane < kDecWarps ? r.qs[lane] : 0);
+  if (blockIdx.x == 0 && tid == 0) {
+    if (a.s_x_out) a.s_x_out[0] = amax;
+    if (a.x_sum_out) a.x_sum_out[0] = *xtot;
+  }
+  return amax;
+}
+
+// R rows of one warp (rows i0 .. i0+R-1 of its group): per-lane partial dot products from
+// the shared-memory copy of the weights, then one warp sum per row.  Words of the lane's
+// range past its K slice meet x = 0 there, so their (arbitrary) weights add nothing.
+template <int JMAX, int R>
+__device__ __forceinline__ void decode_rows(const uint32_t* wsm, int Kw, int G, int gr, int i0, int wbase,
+                                            const uint4 (&xr)[JMAX], int (&tot)[4]) {
+  int acc[R][4];
+#pragma unroll
+  for (int q = 0; q < R; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0;
+#pragma unroll
+  for (int j = 0; j < JMAX; ++j) {
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      const uint32_t w = wsm[(size_t)(gr + (i0 + q) * G) * Kw + wbase + 32 * j];
+      acc[q][0] = dp4a_us(w & 0x03030303u, xr[j].x, acc[q][0]);
+      acc[q][1] = dp4a_us(w & 0x0C0C0C0Cu, xr[j].y, acc[q][1]);
+      acc[q][2] = dp4a_us(w & 0x30303030u, xr[j].z, acc[q][2]);
+      acc[q][3] = dp4a_us(w & 0xC0C0C0C0u, xr[j].w, acc[q][3]);
+    }
+  }
+  // acc_s is 4^s times an integer: the shifts are exact.  tot = sum of c x over the warp's
+  // K slice (c = t + 1); the caller subtracts sum x once per row.
+#pragma unroll
+  for (int q = 0; q < R; ++q)
+    tot[q] = __reduce_add_sync(0xffffffffu, acc[q][0] + (acc[q][1] >> 2) + (acc[q][2] >> 4) + (acc[q][3] >> 6));
+}
+
+// The fused one-token GEMV (see above).  Dynamic shared memory: the CTA's packed rows at
+// offset 0 (then slack for the last row's reads past its slice), xs (a.xs_off), the staged
+// x and gain (a.xf_off), the row totals (a.acc_off, used when S > 1).
+template <int JMAX, int NV, bool RMS>
+__global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = a.K, Kw = K >> 4;
+  const int c = blockIdx.x;
+  const int nrows = a.rows_base + (c < a.rows_rem ? 1 : 0);
+  const int row0 = c * a.rows_base + min(c, a.rows_rem);
+  const uint32_t* wsm = reinterpret_cast<const uint32_t*>(smem);          // [nrows][Kw] packed words
+  uint4* xs = reinterpret_cast<uint4*>(smem + a.xs_off);                 // [Kw] byte-transposed x_q
+  float4* xf4 = reinterpret_cast<float4*>(smem + a.xf_off);              // x [K/4] (+ gain [K/4])
+  int* sacc = reinterpret_cast<int*>(smem + a.acc_off);                  // [nrows] (S > 1)
+  __shared__ DecodeRed red;
+  __shared__ __align__(8) unsigned long long wbar;
+  __shared__ uint32_t red_u[RMS ? kDecWarps : 1];
+  __shared__ unsigned long long red_lo[RMS ? kDecWarps : 1], red_hi[RMS ? kDecWarps : 1];
+  __shared__ float s_inv[1];
+  __shared__ int s_slow[1];
+  __shared__ double s_dbl;
+  __shared__ uint32_t limb[RMS ? 3 : 1][256];
+  __shared__ unsigned long long hist[RMS ? 256 : 1];
+
+  pdl_launch_dependents();
+
+  // ---- the weights, their scale and the RMSNorm gain are parameters: fetch them now
+  const uint32_t bar = smem_addr(&wbar);
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t total = (uint32_t)nrows * (uint32_t)(K >> 2);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(total) : "memory");
+    const unsigned char* src = a.packed + (size_t)row0 * (K >> 2);
+    constexpr uint32_t kChunk = 16384;
+    for (uint32_t off = 0; off < total; off += kChunk) {
+      const uint32_t n = min(kChunk, total - off);
+      asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                       smem_addr(smem + off)),
+                   "l"(src + off), "r"(n), "r"(bar)
+                   : "memory");
+    }
+  }
+  const float gam = __ldg(a.w_scale);
+  const int S = a.S, G = kDecWarps / S;
+  if (S > 1)
+    for (int i = tid; i < nrows; i += kDecThreads) sacc[i] = 0;
+  float4 gv[NV];  // this thread's float4s of the RMSNorm gain (also staged for the other warps)
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    gv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (RMS && tid + q * kDecThreads < (K >> 2)) {
+      gv[q] = __ldg(reinterpret_cast<const float4*>(a.g) + tid + q * kDecThreads);
+      xf4[(K >> 2) + tid + q * kDecThreads] = gv[q];
+    }
+  }
+  // the rows and K slice of this warp
+  const int sl = warp % S, gr = warp / S;
+  const int Ws = (Kw + S - 1) / S;
+  const int ws0 = sl * Ws, ws1 = min(Kw, ws0 + Ws);
+  const int nr = nrows > gr ? (nrows - gr + G - 1) / G : 0;  // rows of this group
+  // x may come from the previous kernel: only prefetched into the coherent L2 before the wait
+  for (int i = tid; i < (K >> 5); i += kDecThreads)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.x + (size_t)i * 32) : "memory");
+  pdl_wait();
+
+  float cs;
+  int xtot;
+  const float amax = decode_prologue<RMS, NV>(a, xs, xf4, gv, red, red_u, red_lo, red_hi, limb, hist, &s_dbl, s_inv,
+                                              s_slow, gam, &cs, &xtot);
+  const bool cs_normal = cs >= 1.17549435e-38f;
+
+  uint4 xr[JMAX];
+#pragma unroll
+  for (int j = 0; j < JMAX; ++j) {
+    const int wi = ws0 + lane + 32 * j;
+    xr[j] = (wi < ws1) ? xs[wi] : make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  // every thread that reads the copied rows waits on the mbarrier (bounded); a warp gives
+  // up only as a whole
+  const bool arrived = __all_sync(0xffffffffu, dec_mbar_wait(bar, 0));
+  if (!arrived && lane == 0) atomicCAS(&g_stream_status, 0, (int)TW_ERR_TIMEOUT);
+
+  auto emit = [&](int i0, int n, const int (&tot)[4]) {
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q < n) {
+          const int rr = gr + (i0 + q) * G;
+          if (S == 1) {
+            const int acc = tot[q] - xtot;
+            a.y[row0 + rr] = cs_normal ? __fmul_rn((float)acc, cs) : dequant_tiny(acc, gam, amax);
+            if (a.acc_out) a.acc_out[row0 + rr] = acc;
+          } else {
+            atomicAdd(&sacc[rr], tot[q]);
+          }
+        }
+      }
+    }
+  };
+  if (arrived) {
+    const int wbase = ws0 + lane;
+    int i0 = 0;
+    int tot[4];
+    if constexpr (JMAX <= 5) {  // four rows at a time while registers allow
+      for (; i0 + 4 <= nr; i0 += 4) {
+        decode_rows<JMAX, 4>(wsm, Kw, G, gr, i0, wbase, xr, tot);
+        emit(i0, 4, tot);
+      }
+    }
+    for (; i0 + 2 <= nr; i0 += 2) {
+      decode_rows<JMAX, 2>(wsm, Kw, G, gr, i0, wbase, xr, tot);
+      emit(i0, 2, tot);
+    }
+    if (i0 < nr) {
+      decode_rows<JMAX, 1>(wsm, Kw, G, gr, i0, wbase, xr, tot);
+      emit(i0, 1, tot);
+    }
+  }
+  if (S > 1) {  // block-uniform
+    if (!__syncthreads_or(!arrived)) {
+      for (int rr = tid; rr < nrows; rr += kDecThreads) {
+        const int acc = sacc[rr] - xtot;
+        a.y[row0 + rr] = dequant(acc, cs, gam, amax);
+        if (a.acc_out) a.acc_out[row0 + rr] = acc;
+      }
+    }
+  }
+  // a CTA that gave up leaves its outputs unwritten, but must not exit while its copies
+  // may still land in shared memory: one more bounded wait
+  if (!arrived) dec_mbar_wait(bar, 0);
+}
+
 }  // namespace tw
 
 namespace {
@@ -608,12 +1058,15 @@ struct Plan {
 };
 
 constexpr int kMaxRowsPerCta = 8192;
+// Dynamic shared memory of the one-token decode kernel: at most this much, so that the
+// next launch's CTA (programmatic dependent launch) fits on the SM beside it.
+constexpr size_t kDecodeSmemMax = 110 * 1024;
 
 // Largest number of 32-bit words of x (per token) a lane keeps in registers.
 int jmax_cap(int MT) { return MT == 1 ? 6 : MT == 2 ? 3 : 2; }
 
 // Returns false when the shape is outside what the streaming kernel handles.
-bool make_plan(int M, int N, int K, int num_sms, Plan& p, bool fused) {
+bool make_plan(int M, int N, int K, int num_sms, Plan& p, bool fused, bool rms = true) {
   const int MT = M <= 1 ? 1 : M <= 2 ? 2 : 4;
   if (M > 4 || K % 64 != 0) return false;
   const int Kw = K / 16;
@@ -643,8 +1096,9 @@ bool make_plan(int M, int N, int K, int num_sms, Plan& p, bool fused) {
   p.xs_off = 0;
   p.acc_off = MT * Kw * 16;
   p.smem = (size_t)p.acc_off + ((size_t)max_rows * MT * 4 + 15) / 16 * 16;
-  // the fused prologue stages x (and the RMSNorm gain) in shared memory when it fits
-  const size_t stage = (size_t)(MT + 1) * K * 4;
+  // the fused prologue stages x (and the RMSNorm gain) in shared memory when it fits; one
+  // token (the decode kernel) may stage more, as long as two CTAs still fit on an SM
+  const size_t stage = (size_t)(MT + (rms ? 1 : 0)) * K * 4;
   p.xf_off = -1;
   if (fused && stage <= 64 * 1024) {
     p.xf_off = (int)p.smem;
@@ -661,6 +1115,8 @@ cudaError_t launch(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, 
   auto kern = tw::gemv_stream_kernel<MT, JMAX, pre_for(MT, JMAX), FUSED, RMS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);
   cfg.blockDim = dim3(tw::kThreads);
@@ -672,6 +1128,100 @@ cudaError_t launch(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, 
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Launch plan of the one-token decode kernel: one CTA per SM (the other slot is left to the
+// next launch), the CTA's packed rows, x_q, the staged x (and gain) and the row totals in
+// dynamic shared memory.  False when that does not fit in kDecodeSmemMax.
+bool make_decode_plan(int N, int K, int num_sms, bool rms, Plan& p) {
+  if (K % 64 != 0 || K > 16384) return false;
+  const int Kw = K / 16;
+  p.S = 0;
+  for (int S : {1, 2, 4, 8, 16}) {  // divisors of the decode kernel's warp count
+    const int Ws = (Kw + S - 1) / S;
+    if ((Ws + 31) / 32 <= 8) {
+      p.S = S;
+      p.jmax = (Ws + 31) / 32;
+      break;
+    }
+  }
+  if (p.S == 0) return false;
+  p.grid = N < num_sms ? N : num_sms;
+  p.rows_base = N / p.grid;
+  p.rows_rem = N % p.grid;
+  const size_t max_rows = (size_t)p.rows_base + (p.rows_rem ? 1 : 0);
+  auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
+  // the last row's lanes read up to S * 32 * jmax - Kw words past its end (against x = 0)
+  const size_t slack = (size_t)(p.S * 32 * p.jmax - Kw) * 4;
+  size_t off = up(max_rows * (size_t)(K / 4) + slack, 128);
+  p.xs_off = (int)off;
+  off = up(off + (size_t)K, 16);
+  p.xf_off = (int)off;
+  off += (size_t)(rms ? 2 : 1) * K * 4;
+  p.acc_off = (int)off;
+  off += p.S > 1 ? up(max_rows * 4, 16) : 0;
+  p.smem = off;
+  return p.smem <= kDecodeSmemMax;
+}
+
+template <int JMAX, int NV, bool RMS>
+cudaError_t launch_decode(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, bool pdl) {
+  auto kern = tw::gemv_decode_kernel<JMAX, NV, RMS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  // every kernel of a decode chain asks for the same (largest) shared-memory carveout, so
+  // that the next launch's CTA can join an SM whatever the shared memory of the running one
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid);
+  cfg.blockDim = dim3(tw::kDecThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// The kernel's template arguments follow from the plan: JMAX = words per lane and row, NV =
+// float4s of x per thread, ceil(K / 4 / kDecThreads): 2 when one warp spans K (S = 1), up to 4
+// with two K slices, up to 8 with four (the plan admits K <= 16384).
+template <bool RMS>
+cudaError_t dispatch_decode(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, bool pdl) {
+  const int nv = (a.K / 4 + tw::kDecThreads - 1) / tw::kDecThreads;
+  if (nv <= 2) {
+    switch (p.jmax) {
+      case 1: return launch_decode<1, 2, RMS>(a, p, stream, pdl);
+      case 2: return launch_decode<2, 2, RMS>(a, p, stream, pdl);
+      case 3: return launch_decode<3, 2, RMS>(a, p, stream, pdl);
+      case 4: return launch_decode<4, 2, RMS>(a, p, stream, pdl);
+      case 5: return launch_decode<5, 2, RMS>(a, p, stream, pdl);
+      case 6: return launch_decode<6, 2, RMS>(a, p, stream, pdl);
+      case 7: return launch_decode<7, 2, RMS>(a, p, stream, pdl);
+      case 8: return launch_decode<8, 2, RMS>(a, p, stream, pdl);
+      default: break;
+    }
+  } else if (nv <= 4) {
+    switch (p.jmax) {
+      case 5: return launch_decode<5, 4, RMS>(a, p, stream, pdl);
+      case 6: return launch_decode<6, 4, RMS>(a, p, stream, pdl);
+      case 7: return launch_decode<7, 4, RMS>(a, p, stream, pdl);
+      case 8: return launch_decode<8, 4, RMS>(a, p, stream, pdl);
+      default: break;
+    }
+  } else if (nv <= 8) {
+    switch (p.jmax) {
+      case 5: return launch_decode<5, 8, RMS>(a, p, stream, pdl);
+      case 6: return launch_decode<6, 8, RMS>(a, p, stream, pdl);
+      case 7: return launch_decode<7, 8, RMS>(a, p, stream, pdl);
+      case 8: return launch_decode<8, 8, RMS>(a, p, stream, pdl);
+      default: break;
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int MT, bool FUSED, bool RMS>
@@ -725,13 +1275,18 @@ cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, cons
                                  float* s_x_out, int32_t* x_sum_out, int32_t* acc_out, cudaStream_t stream,
                                  int num_sms, bool pdl) {
   Plan p;
-  if (!make_plan(M, N, K, num_sms, p, true)) return cudaErrorInvalidValue;
+  if (!make_plan(M, N, K, num_sms, p, true, g != nullptr)) return cudaErrorInvalidValue;
   tw::StreamArgs a = {};
   a.packed = packed; a.w_scale = w_scale; a.x = x; a.g = g; a.eps = eps; a.kd = tw::make_kdiv(K);
   a.inv_k = 1.0f / (float)K;
   a.M = M; a.N = N; a.K = K; a.y = y; a.acc_out = acc_out;
   a.x_q_out = x_q_out; a.s_x_out = s_x_out; a.x_sum_out = x_sum_out;
   fill_plan(a, p);
+  Plan dp;
+  if (M == 1 && make_decode_plan(N, K, num_sms, g != nullptr, dp)) {  // one token: the decode kernel
+    fill_plan(a, dp);
+    return g ? dispatch_decode<true>(a, dp, stream, pdl) : dispatch_decode<false>(a, dp, stream, pdl);
+  }
   if (g) return dispatch<true, true>(a, p, stream, pdl);
   return dispatch<true, false>(a, p, stream, pdl);
 }

@@ -384,6 +384,80 @@ def test_quant_gemv_chain_pdl(tw):
         assert_y_close(host(bufs[i + 1]), ref[i + 1])
 
 
+def _decode_case_check(tw, x, g, N=640, seed=0):
+    """One-token fused launch (RMSNorm) on x [1][K] with gain g, against the oracle."""
+    K = x.shape[1]
+    W = si.weights(N, K, seed=seed)
+    p_ref, g_ref = oracle.pack_ternary(W)
+    q_ref, s_ref, sum_ref = oracle.rmsnorm_quant_act(x, g, si.RMS_EPS)
+    y_ref, acc_ref = oracle.ternary_matmul(p_ref, g_ref, q_ref, s_ref)
+    y, acc, xq, sx, xs, y2 = fused_run(tw, x, p_ref, g_ref, g)
+    assert (xq == q_ref).all()
+    assert (sx.view(np.uint32) == s_ref.view(np.uint32)).all()
+    assert (xs == sum_ref).all() and (acc == acc_ref).all()
+    assert_y_close(y, y_ref)
+    assert (y2 == y).all()
+
+
+def _inv_rms_f32(x_row, eps):
+    """fl32 RMSNorm scale of one row, for building test inputs (not a check): exact sum of
+    squares (math.fsum of exact double squares), one rounding to fp32 of the mean, IEEE
+    fp32 square root and divide."""
+    import math
+    f32 = np.float32
+    ms = f32(math.fsum(float(v) * float(v) for v in x_row) / len(x_row))
+    return f32(1.0) / np.sqrt(f32(ms + f32(eps)))
+
+
+def test_decode_scale_candidate_not_the_maximum(tw):
+    """One token with RMSNorm: the element with the largest fl(|x g|) is not the one with the
+    largest |u| = fl(fl(x inv) g) (two products a fraction of an ulp apart whose roundings
+    cross).  The one-token kernel takes the first as its candidate scale and must notice
+    that another |u| exceeds it."""
+    f32 = np.float32
+    K = 2560
+    rng = np.random.default_rng(11)
+    x = si.activations(1, K, seed=901)
+    g = si.rms_gain(K, seed=902)
+    i, j = 100, 1700
+    for _ in range(200000):
+        xi, gi = f32(rng.uniform(7, 9)), f32(rng.uniform(1.1, 1.3))
+        xj = f32(xi * (1 + rng.uniform(-3, 3) * 2.0 ** -23))
+        gj = f32(gi * (1 + rng.uniform(-3, 3) * 2.0 ** -23))
+        x[0, i], g[i], x[0, j], g[j] = xi, gi, xj, gj
+        inv = _inv_rms_f32(x[0], si.RMS_EPS)
+        p_i, p_j = abs(f32(xi * gi)), abs(f32(xj * gj))
+        u_i, u_j = abs(f32(f32(xi * inv) * gi)), abs(f32(f32(xj * inv) * gj))
+        if p_i > p_j and u_j > u_i:
+            break
+    else:
+        pytest.fail("no crossing pair found")
+    assert np.abs(x[0] * g).argmax() == i  # the candidate is element i ...
+    _decode_case_check(tw, x, g)
+    _, s_ref, _ = oracle.rmsnorm_quant_act(x, g, si.RMS_EPS)
+    assert s_ref[0] == u_j  # ... and the scale is element j's
+
+
+@pytest.mark.parametrize("kind", ["underflow", "ties", "zero_gain"])
+def test_decode_scale_edge_rows(tw, kind):
+    """One token with RMSNorm where the products |x g| tell nothing about max |u|: they
+    underflow to zero while u does not; many exactly equal products; an all-zero gain."""
+    K = 2560
+    x = si.activations(1, K, seed=903)
+    g = si.rms_gain(K, seed=904)
+    if kind == "underflow":  # |x g| < 2^-150 but x inv g is a nonzero subnormal or small normal
+        x = (x * np.float32(5e-21)).astype(np.float32)
+        g = (g * np.float32(1e-26)).astype(np.float32)
+        assert (np.float32(np.abs(x) * np.abs(g)) == 0).all()
+    elif kind == "ties":  # every |x| equal: all products tie in exact arithmetic on 1/g
+        x = np.where(x >= 0, np.float32(3.0), np.float32(-3.0)).astype(np.float32)
+        g = np.float32(0.75) * np.ones(K, np.float32)
+        g[::7] = np.float32(0.7500001)
+    else:
+        g = np.zeros(K, np.float32)
+    _decode_case_check(tw, x, g)
+
+
 @pytest.mark.parametrize("M", [1, 2, 4])
 def test_long_stream_two_ctas_per_sm(tw, M):
     """A matrix with more rows than one register batch of every warp (the kernel then runs
