@@ -8,6 +8,7 @@ invariants of the method.
 """
 import math
 import os
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -188,6 +189,105 @@ def test_act_quant_golden_ties():
         assert xq[0].tolist() == [int(v) for v in right]
         assert sx[0] == np.abs(x).max()
         assert xs[0] == sum(int(v) for v in right)
+
+
+# Exact rational arithmetic for re-deriving the hand-worked fixtures: fp32 values as
+# Fractions, IEEE round-to-nearest-even onto the fp32 grid, a correctly rounded square root
+# (checked against the squares of the neighbouring midpoints) and round-half-even to an
+# integer.  None of it comes from the oracle.
+def _ex(v):
+    return Fraction(float(np.float32(v)))
+
+
+def _fl32(q):
+    if q == 0:
+        return Fraction(0)
+    sign = -1 if q < 0 else 1
+    q = abs(q)
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1
+    if Fraction(2) ** (e + 1) <= q:
+        e += 1
+    step = Fraction(1, 2 ** 149) if e < -126 else Fraction(2) ** (e - 23)
+    n = q / step
+    return sign * _rne(n) * step
+
+
+def _rne(q):
+    f = q.numerator // q.denominator
+    r = q - f
+    return f + (1 if r > Fraction(1, 2) or (r == Fraction(1, 2) and f % 2 == 1) else 0)
+
+
+def _next32(v, up):
+    return Fraction(float(np.nextafter(np.float32(float(v)), np.float32(np.inf if up else -np.inf))))
+
+
+def _sqrt32(t):
+    c = Fraction(float(np.float32(math.sqrt(float(t)))))
+    for cand in (_next32(c, False), c, _next32(c, True)):
+        lo, hi = (_next32(cand, False) + cand) / 2, (cand + _next32(cand, True)) / 2
+        if lo * lo < t < hi * hi:
+            return cand
+    raise AssertionError("no fp32 square root found")
+
+
+def test_act_quant_golden_order():
+    """Tokens where fl(fl(x*127)/a) sits exactly on a half-integer: the oracle must take
+    the tie to even, and the reciprocal form must land elsewhere (so the fixture tells
+    the two orders apart)."""
+    for left, right in _golden_rows("act_quant_order.txt"):
+        x = np.array([float(v) for v in left], np.float32)
+        expect = [int(v) for v in right]
+        a = max(abs(_ex(v)) for v in x)
+        derived = [_rne(_fl32(_fl32(_ex(v) * 127) / a)) for v in x]
+        assert derived == expect  # the fixture agrees with its exact derivation
+        recip = _fl32(Fraction(127) / a)
+        assert [_rne(_fl32(_ex(v) * recip)) for v in x] != expect
+        xq, sx, xs = oracle.quant_act(x)
+        assert xq[0].tolist() == expect
+        assert sx[0] == np.float32(float(a)) and xs[0] == sum(expect)
+
+
+def test_rmsnorm_golden_k4():
+    """One K = 4 token with every fp32 step of the RMSNorm reading pinned (u bits and x_q),
+    re-derived here with exact rationals; the one-rounding inverse and the (x*g)*inv order
+    both give a different x_q on it."""
+    rows = []
+    with open(os.path.join(GOLDEN, "rmsnorm_k4.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([part.split() for part in line.split("|")])
+    assert rows
+    eps = np.float32(si.RMS_EPS)
+    for xs_, gs_, ubits_, q_ in rows:
+        x = np.array([float(v) for v in xs_], np.float32)
+        g = np.array([float(v) for v in gs_], np.float32)
+        ubits = np.array([int(v) for v in ubits_], np.uint32)
+        expect = [int(v) for v in q_]
+        # exact derivation of the reading
+        r = sum(_ex(v) ** 2 for v in x)
+        ms = _fl32(r / len(x))
+        inv = _fl32(1 / _sqrt32(_fl32(ms + _ex(eps))))
+        u = [_fl32(_fl32(_ex(xv) * inv) * _ex(gv)) for xv, gv in zip(x, g)]
+        assert [int(np.float32(float(v)).view(np.uint32)) for v in u] == ubits.tolist()
+        a = max(abs(v) for v in u)
+        assert [_rne(_fl32(_fl32(v * 127) / a)) for v in u] == expect
+        # the oracle
+        u_o, r_o = oracle.rmsnorm(x, g, eps)
+        assert r_o[0] == float(r)
+        assert (u_o[0].view(np.uint32) == ubits).all()
+        xq, sx, _ = oracle.rmsnorm_quant_act(x, g, eps)
+        assert xq[0].tolist() == expect and sx[0] == np.float32(float(a))
+        # the other readings differ on this row
+        t = np.float32(float(_fl32(ms + _ex(eps))))
+        inv_one = np.float32(1.0 / math.sqrt(float(t)))
+        for uu in ([np.float32(np.float32(xv * inv_one) * gv) for xv, gv in zip(x, g)],
+                   [np.float32(np.float32(xv * gv) * np.float32(float(inv))) for xv, gv in zip(x, g)]):
+            aa = max(abs(v) for v in uu)
+            alt = [int(np.rint(np.float32(np.float32(v * np.float32(127)) / aa))) for v in uu]
+            assert alt != expect
 
 
 def test_act_quant_invariants():
