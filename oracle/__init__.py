@@ -19,8 +19,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "tw_oracle.c")
 _LIB = os.path.join(_HERE, "libtw_oracle.so")
+_LIB_OMP = os.path.join(_HERE, "libtw_oracle_omp.so")  # the same source built with -fopenmp
 _lock = threading.Lock()
 _lib = None
+_lib_omp = None
 
 # gcc flags: one IEEE rounding per fp32 operation (no contraction, no fast-math).
 CFLAGS = ["-O2", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off",
@@ -36,38 +38,55 @@ class OracleError(RuntimeError):
         self.code = code
 
 
-def build(force: bool = False) -> str:
-    """Compile libtw_oracle.so with gcc (if missing or older than the source)."""
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile libtw_oracle.so with gcc (if missing or older than the source).  openmp=True
+    builds libtw_oracle_omp.so instead: the same source with -fopenmp, whose integer product
+    shares its output rows out over the host's cores (the all-core CPU baseline)."""
+    lib = _LIB_OMP if openmp else _LIB
     with _lock:
-        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-            tmp = _LIB + f".tmp{os.getpid()}"
-            subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
-            os.replace(tmp, _LIB)
-    return _LIB
+        if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(_SRC):
+            tmp = lib + f".tmp{os.getpid()}"
+            subprocess.check_call(["gcc", *CFLAGS, *(["-fopenmp"] if openmp else []), "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, lib)
+    return lib
 
 
-def _load():
-    global _lib
+def _load(openmp: bool = False):
+    global _lib, _lib_omp
+    if openmp:
+        if _lib_omp is None:
+            _lib_omp = _bind(ctypes.CDLL(build(openmp=True)))
+        return _lib_omp
     if _lib is None:
-        lib = ctypes.CDLL(build())
-        i64, p = ctypes.c_int64, ctypes.c_void_p
-        sig = {
-            "two_exact_sum": [p, i64, p],
-            "two_absmean": [p, i64, p, p],
-            "two_pack_rows_with_scale": [p, i64, i64, ctypes.c_float, p],
-            "two_pack_ternary": [p, i64, i64, p, p],
-            "two_unpack_ternary": [p, i64, i64, p],
-            "two_quant_act": [p, i64, i64, p, p, p],
-            "two_rmsnorm": [p, p, ctypes.c_float, i64, i64, p, p],
-            "two_rmsnorm_quant_act": [p, p, ctypes.c_float, i64, i64, p, p, p],
-            "two_ternary_matmul": [p, ctypes.c_float, p, p, i64, i64, i64, p, p],
-        }
-        for name, args in sig.items():
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = ctypes.c_int
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def _bind(lib):
+    """Argument and result types of the exported functions."""
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    sig = {
+        "two_exact_sum": [p, i64, p],
+        "two_absmean": [p, i64, p, p],
+        "two_pack_rows_with_scale": [p, i64, i64, ctypes.c_float, p],
+        "two_pack_ternary": [p, i64, i64, p, p],
+        "two_unpack_ternary": [p, i64, i64, p],
+        "two_quant_act": [p, i64, i64, p, p, p],
+        "two_rmsnorm": [p, p, ctypes.c_float, i64, i64, p, p],
+        "two_rmsnorm_quant_act": [p, p, ctypes.c_float, i64, i64, p, p, p],
+        "two_ternary_matmul": [p, ctypes.c_float, p, p, i64, i64, i64, p, p],
+        "two_threads": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    return lib
+
+
+def threads(openmp: bool = True) -> int:
+    """Threads the integer product uses (1 for the plain build)."""
+    return int(_load(openmp).two_threads())
 
 
 def _ptr(a):
@@ -167,8 +186,9 @@ def rmsnorm_quant_act(x, g, eps):
     return xq, sx, xs
 
 
-def ternary_matmul(packed, w_scale, x_q, s_x):
-    """packed [N][K/4], x_q int8 [M][K] -> (y fp32 [M][N], acc int32 [M][N])."""
+def ternary_matmul(packed, w_scale, x_q, s_x, openmp: bool = False):
+    """packed [N][K/4], x_q int8 [M][K] -> (y fp32 [M][N], acc int32 [M][N]).  openmp=True
+    runs the all-core build (same results)."""
     packed = _c(packed, np.uint8)
     x_q = _c(x_q, np.int8)
     if x_q.ndim == 1:
@@ -178,6 +198,6 @@ def ternary_matmul(packed, w_scale, x_q, s_x):
     N = packed.shape[0]
     y = np.zeros((M, N), np.float32)
     acc = np.zeros((M, N), np.int32)
-    _check(_load().two_ternary_matmul(_ptr(packed), float(w_scale), _ptr(x_q), _ptr(s_x),
-                                      M, N, K, _ptr(y), _ptr(acc)), "ternary_matmul")
+    _check(_load(openmp).two_ternary_matmul(_ptr(packed), float(w_scale), _ptr(x_q), _ptr(s_x),
+                                            M, N, K, _ptr(y), _ptr(acc)), "ternary_matmul")
     return y, acc

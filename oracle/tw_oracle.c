@@ -47,6 +47,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 enum {
   TWO_OK = 0,
@@ -300,27 +303,50 @@ int two_rmsnorm_quant_act(const float *x, const float *g, float eps, int64_t M,
 /* ------------------------------------------------------------------------ */
 /* Integer ternary product and dequantisation ([P3] 1.1: sign check + add).  */
 /* ------------------------------------------------------------------------ */
+/* Output rows are independent: with -fopenmp (the all-core CPU baseline build) they are
+ * shared out over threads; every output is still the same sum in the same order. */
 int two_ternary_matmul(const uint8_t *packed, float w_scale, const int8_t *x_q,
                        const float *s_x, int64_t M, int64_t N, int64_t K, float *y,
                        int32_t *acc_out) {
   if (!packed || !x_q || !s_x || !y) return TWO_ERR_NULL;
   if (M <= 0 || N <= 0 || K <= 0 || K % 4 != 0) return TWO_ERR_SHAPE;
+  int status = TWO_OK;
   for (int64_t m = 0; m < M; ++m) {
+#pragma omp parallel for schedule(static)
     for (int64_t n = 0; n < N; ++n) {
       int64_t acc = 0;
+      int bad = TWO_OK;
       for (int64_t k = 0; k < K; ++k) {
         unsigned byte = packed[n * (K / 4) + k / 4];
         unsigned code = (byte >> (2 * (k % 4))) & 3u;
-        if (code == 3u) return TWO_ERR_INVALID_CODE;
+        if (code == 3u) {
+          bad = TWO_ERR_INVALID_CODE;
+          break;
+        }
         int t = (int)code - 1;
         int xv = x_q[m * K + k];
         if (t == 1) acc += xv;       /* +1: add */
         else if (t == -1) acc -= xv; /* -1: subtract; 0: skip */
       }
-      if (acc > INT32_MAX || acc < INT32_MIN) return TWO_ERR_OVERFLOW;
+      if (bad == TWO_OK && (acc > INT32_MAX || acc < INT32_MIN)) bad = TWO_ERR_OVERFLOW;
+      if (bad != TWO_OK) {
+#pragma omp atomic write
+        status = bad;
+        continue;
+      }
       if (acc_out) acc_out[m * N + n] = (int32_t)acc;
       y[m * N + n] = (float)(((double)acc * (double)w_scale * (double)s_x[m]) / 127.0);
     }
+    if (status != TWO_OK) return status;
   }
   return TWO_OK;
+}
+
+/* Threads the row loop above may use: 1 in the plain build. */
+int two_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
 }

@@ -16,6 +16,7 @@ def pytest_configure(config):
     __graft_entry__._build_module().build()
     import oracle
     oracle.build()
+    oracle.build(openmp=True)
 
 
 def pytest_collection_modifyitems(config, items):

@@ -53,8 +53,25 @@ def test_reference_arm_json_line():
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference"
     assert line["unit"] == "GB/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    import oracle
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] == oracle.threads(openmp=True) >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_single_and_all_core():
+    """The CPU baseline reports the all-core rate with its thread count and the single-thread
+    rate beside it, measured on a bounded row sample of the workload's layer."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    assert bench.sample_rows(13824, 2560, 1) == 7812
+    assert bench.sample_rows(2560, 6912, 256) == 16 and bench.sample_rows(256, 256, 1) == 256
+    cb = bench.cpu_baseline_for("2B", 1, 0.0, 0.0)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0
+    assert cb["cores"] == oracle.threads(openmp=True)
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+    assert "rows multiplied per matrix" in cb["sample"]
 
 
 def test_step_bytes_match_layer_shapes():

@@ -395,6 +395,22 @@ def test_matmul_invariants():
     assert (y2 == 2 * y).all()
 
 
+def test_matmul_all_core_build_is_identical():
+    """The all-core (OpenMP over output rows) build of the integer product used for the
+    CPU baseline returns the same accumulators and outputs bit for bit."""
+    W, x = si.gemv_case(5, 301, 640, seed=31, outliers=True)
+    p, g = oracle.pack_ternary(W)
+    q, s, _ = oracle.quant_act(x)
+    y1, a1 = oracle.ternary_matmul(p, g, q, s)
+    y2, a2 = oracle.ternary_matmul(p, g, q, s, openmp=True)
+    assert (a1 == a2).all() and (y1.view(np.uint32) == y2.view(np.uint32)).all()
+    assert oracle.threads(openmp=False) == 1 and oracle.threads(openmp=True) >= 1
+    bad = p.copy()
+    bad[7, 3] |= 0x30  # a code 3 in row 7
+    with pytest.raises(oracle.OracleError):
+        oracle.ternary_matmul(bad, g, q, s, openmp=True)
+
+
 def test_matmul_rejects_invalid_code():
     packed = np.array([[0xFF]], np.uint8)
     with pytest.raises(oracle.OracleError):
