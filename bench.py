@@ -238,71 +238,109 @@ def host_cpu() -> str:
     return f"{model}, {os.cpu_count()} logical cores on the host"
 
 
-def oracle_layer_sample(layer_data, seconds_min: float, seconds_max: float):
-    """Run the oracle's decode-layer sequence over host copies of layers until >= seconds_min.
+def sample_rows(N: int, K: int, M: int, budget: float = 2e7) -> int:
+    """Rows of an N x K matrix the CPU oracle multiplies in one pass of its bounded sample:
+    about `budget` weight-token products per matrix (at least 16 rows, at most all)."""
+    return int(max(16, min(N, budget // max(1, M * K))))
 
-    Returns (bytes processed, elapsed seconds, layers run)."""
+
+def host_oracle_layer(model: str, M: int, seed: int = 4242, outliers: bool = False):
+    """One layer of seeded host inputs for the CPU oracle, with the GPU workload's shapes and
+    recipe; per matrix only sample_rows() rows are drawn (the oracle's rate per byte is what is
+    measured, and its time per row does not depend on which rows)."""
+    import oracle
+    import seeded_inputs as si
+    g = si.cpu_generator(seed)
+    L = []
+    for name, N, K, pro in layer_plan(model):
+        rows = sample_rows(N, K, M)
+        packed, gamma = oracle.pack_ternary(si.weights(rows, K, gen=g))
+        L.append(dict(name=name, N=N, K=K, pro=pro, rows=rows, packed=packed, gamma=gamma,
+                      x=si.activations(M, K, gen=g, outliers=outliers),
+                      g=si.rms_gain(K, seed=seed) if pro == "rms" else None))
+    return L
+
+
+def oracle_rate(L, M: int, seconds: float, openmp: bool):
+    """The oracle's decode-layer sequence (RMSNorm/quantisation of the M tokens, then the
+    integer product of each matrix) repeated for at least `seconds`.  Each product's time is
+    scaled by N / rows to the full matrix; returns (GB/s of the metric's bytes, passes)."""
     import oracle
     import seeded_inputs as si
     t0 = time.perf_counter()
-    done_bytes, n = 0, 0
-    plan = layer_plan()
+    full_time, full_bytes, passes = 0.0, 0, 0
     while True:
-        L = layer_data[n % len(layer_data)]
-        for name, N, K, pro in plan:
-            x = L["x"][name]
-            if pro == "rms":
-                xq, sx, _ = oracle.rmsnorm_quant_act(x, L["g"][name], si.RMS_EPS)
+        for e in L:
+            a = time.perf_counter()
+            if e["pro"] == "rms":
+                xq, sx, _ = oracle.rmsnorm_quant_act(e["x"], e["g"], si.RMS_EPS)
             else:
-                xq, sx, _ = oracle.quant_act(x)
-            oracle.ternary_matmul(L["packed"][name], L["gamma"][name], xq, sx)
-            done_bytes += gemv_bytes(N, K)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds_min or el >= seconds_max:
-            return done_bytes, el, n
+                xq, sx, _ = oracle.quant_act(e["x"])
+            b = time.perf_counter()
+            oracle.ternary_matmul(e["packed"], e["gamma"], xq, sx, openmp=openmp)
+            c = time.perf_counter()
+            full_time += (b - a) + (c - b) * e["N"] / e["rows"]
+            full_bytes += gemv_bytes(e["N"], e["K"], M)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            return full_bytes / full_time / 1e9, passes
 
 
-def host_oracle_layers(n_layers: int, seed: int = 4242):
-    """Seeded host inputs for the oracle sample: same shapes and recipe as the GPU workload."""
+def cpu_baseline_for(model: str, M: int, seconds_single: float, seconds_all: float, outliers: bool = False):
+    """The oracle as a CPU baseline of one workload: single thread, then all host cores (the
+    OpenMP build of its integer product).  `value` is the all-core rate."""
+    import oracle
+    L = host_oracle_layer(model, M, outliers=outliers)
+    single, n1 = oracle_rate(L, M, seconds_single, openmp=False)
+    cores = oracle.threads(openmp=True)
+    allc, n2 = oracle_rate(L, M, seconds_all, openmp=True)
+    rows = ", ".join(f"{e['name']} {e['rows']}/{e['N']}" for e in L)
+    return {"value": allc, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "single_thread": {"value": single, "cores": 1, "passes": n1},
+            "sample": (f"{n2} pass(es) all-core and {n1} single-thread over one {model}-shaped layer at "
+                       f"M = {M} (quantisation + the four products); rows multiplied per matrix: {rows}, "
+                       f"each product's time scaled by N / rows; {host_cpu()}")}
+
+
+def cpu_small_case_us(reps: int = 2000):
+    """The small configuration (K = N = 256, M = 1) on the oracle: microseconds per call
+    (quantisation + integer product), single thread."""
     import oracle
     import seeded_inputs as si
-    out = []
-    for l in range(n_layers):
-        g = si.cpu_generator(seed + l)
-        L = {"packed": {}, "gamma": {}, "x": {}, "g": {}}
-        for name, N, K, pro in layer_plan():
-            W = si.weights(N, K, gen=g)
-            L["packed"][name], L["gamma"][name] = oracle.pack_ternary(W)
-            L["x"][name] = si.activations(1, K, gen=g)
-            if pro == "rms":
-                L["g"][name] = si.rms_gain(K, seed=seed + l)
-        out.append(L)
-    return out
+    W, x = si.gemv_case(1, 256, 256, seed=0)
+    p, g = oracle.pack_ternary(W)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        xq, sx, _ = oracle.quant_act(x)
+        oracle.ternary_matmul(p, g, xq, sx)
+    return (time.perf_counter() - t0) / reps * 1e6
 
 
 def run_reference(args):
+    """The oracle (the plain CPU implementation of the same path) as the reference arm: each
+    step is one bounded pass over a row sample of the default workload on all host cores."""
+    import oracle
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    layers = host_oracle_layers(1)
+    L = host_oracle_layer(MODEL, 1)
     for _ in range(args.warmup):
-        oracle_layer_sample(layers, 0.0, 0.0)
+        oracle_rate(L, 1, 0.0, openmp=True)
     t0 = time.perf_counter()
-    total_bytes = 0
-    for _ in range(args.steps):
-        b, _, _ = oracle_layer_sample(layers, 0.0, 0.0)  # one layer per step
-        total_bytes += b
+    rates = [oracle_rate(L, 1, 0.0, openmp=True)[0] for _ in range(args.steps)]
     el = time.perf_counter() - t0
-    value = total_bytes / el / 1e9
+    value = statistics.median(rates)
+    cores = oracle.threads(openmp=True)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD + "; oracle step = one layer (bounded sample)", "M": 1},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "one 2B-shaped layer per step (RMSNorm/quant + 4 GEMVs), single thread; "
-                                       + host_cpu()},
+            "config": {"workload": WORKLOAD + "; oracle step = one pass over a row sample of one layer",
+                       "M": 1},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": ("one pass per step over one 2B-shaped layer (quantisation + four "
+                                        "products), rows sampled per matrix, product times scaled to the "
+                                        "full matrix; all cores (OpenMP over output rows); " + host_cpu())},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -500,64 +538,64 @@ def read_stream_rate(gib: float = 2.0):
     return {"GB/s": gbs, "how": "torch.amax over a 2 GiB fp32 buffer, 5 passes"}
 
 
-def run_ours(args):
+def measure(tw, workload: str, steps: int, warmup: int, world: int, separate: bool = False, clocks=None,
+            e2e_steps: int = 500):
+    """GPU measurement of one workload: its decode-layer stack captured in one CUDA graph and
+    replayed `steps` times (CUDA events on the replaying stream); the roofline of the product
+    kernel; the same metric end to end (inputs from and outputs to pinned host memory inside
+    the timed region).  Returns (result dict, stack, graph, fused)."""
     import torch
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    import ternary_weight_quant_b300 as tw
-
-    model, layers, M, distinct = WORKLOADS[args.workload]
+    model, layers, M, distinct = WORKLOADS[workload]
     # one token: quantisation fused into the GEMV launch; 2-4 tokens: separate kernels, which
     # measured faster (70B at 4 tokens: 241.6 against 275.4 us per layer; the fused prologue
     # quantises its tokens one after another)
-    fused = (not args.separate) and M == 1
+    fused = (not separate) and M == 1
     stack = DecodeStack(tw, layers, M=M, model=model, distinct=distinct)
     plan = layer_plan(model)
     bytes_per_step = step_bytes(M, model, layers)
     ops_per_step = step_ops(M, model, layers)
     graph = capture(stack, fused)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize()
 
-    # ---- timed region: K graph replays
+    # ---- timed region: `steps` graph replays
     start, stop = events_new(), events_new()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_wall0 = time.perf_counter()
-        start.record()
-        for _ in range(args.steps):
-            graph.replay()
-        stop.record()
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
+    t_wall0 = time.perf_counter()
+    if clocks is not None:
+        clocks.__enter__()
+    start.record()
+    for _ in range(steps):
+        graph.replay()
+    stop.record()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.__exit__(None, None, None)
+    t_wall = time.perf_counter() - t_wall0
     barrier(world)
     elapsed = start.elapsed_time(stop) / 1e3
-    elapsed_max, total_bytes = combine_over_ranks(elapsed, bytes_per_step * args.steps, world)
+    elapsed_max, total_bytes = combine_over_ranks(elapsed, bytes_per_step * steps, world)
     value = total_bytes / elapsed_max / 1e9
-    ms_per_step = elapsed_max / args.steps * 1e3
-    us_per_layer = ms_per_step * 1e3 / layers
+    ms_per_step = elapsed_max / steps * 1e3
 
     # ---- roofline of the product kernel.  Fused: every launch of the step is the product
     # kernel, so its average launch duration is the timed region over its launches.  Otherwise
     # a second graph holds only the product calls (the quantised inputs stay from earlier
     # steps) and is replayed as many times as the timed region, timed the same way.
-    shapes = {name: (N, K) for name, N, K, _ in plan}
     peak_hbm, peak_kind = measured_peaks()
     prod_calls_per_step = layers * len(plan)
-    whole_step = fused and all(stack.fused_ok(stack.L[0][n]) for n in shapes)
+    whole_step = fused and all(stack.fused_ok(stack.L[0][n]) for n, _, _, _ in plan)
     if whole_step:
         prod_elapsed = elapsed
     else:
         pgraph = capture(stack, fused, product_only=True)
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             pgraph.replay()
-        prod_elapsed = timed_replays(pgraph, args.steps, world)
-    avg_launch_s = prod_elapsed / (args.steps * prod_calls_per_step)
+        prod_elapsed = timed_replays(pgraph, steps, world)
+        del pgraph
+    avg_launch_s = prod_elapsed / (steps * prod_calls_per_step)
     if M <= 16:
         algo_per_call = bytes_per_step / prod_calls_per_step
         achieved, peak, unit, bound = algo_per_call / avg_launch_s / 1e9, peak_hbm, "GB/s", "hbm"
@@ -565,23 +603,12 @@ def run_ours(args):
         algo_per_call = ops_per_step / prod_calls_per_step
         peak, pk = measured_tensor_peak()
         achieved, unit, bound, peak_kind = algo_per_call / avg_launch_s / 1e12, "TFLOP/s", "tensor", pk
-
-    # per shape, each call on its own: events around each product call of extra steps enqueued
-    # behind a short GPU sleep (host launch overhead hidden; no overlap with the next call)
-    per_launch = {}
-    for rep in range(3):
-        evs = []
-        gpu_sleep(30.0)
-        stack.enqueue(events=evs, fused=fused)
-        torch.cuda.synchronize()
-        if rep == 0:
-            continue
-        for name, a, b in evs:
-            per_launch.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
-    per_shape = {n: {"bytes": gemv_bytes(*shapes[n], M), "us_median": statistics.median(v) * 1e6,
-                     "GB/s": gemv_bytes(*shapes[n], M) / statistics.median(v) / 1e9,
-                     "TFLOP/s": 2 * M * shapes[n][0] * shapes[n][1] / statistics.median(v) / 1e12}
-                 for n, v in per_launch.items()}
+    if fused:
+        kern = "tw::gemv_decode_kernel (one token, quantisation fused)"
+    elif M <= 16:
+        kern = "tw::gemv_stream_kernel / gemv_dp4a_kernel"
+    else:
+        kern = "tw::gemm::gemm_tok_kernel / gemm_tma_kernel (tcgen05)"
 
     # ---- e2e: inputs from pinned host, outputs back to pinned host, per step (one copy each way)
     h_in = stack.x_all.cpu().pin_memory()
@@ -597,21 +624,85 @@ def run_ours(args):
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_steps = max(1, min(args.steps, 500))
+    n_e2e = max(1, min(steps, e2e_steps))
     barrier(world)
     e0, e1 = events_new(), events_new()
     e0.record()
-    for _ in range(e2e_steps):
+    for _ in range(n_e2e):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_el, e2e_bytes = combine_over_ranks(e0.elapsed_time(e1) / 1e3, bytes_per_step * e2e_steps, world)
-    e2e_value = e2e_bytes / e2e_el / 1e9
+    e2e_el, e2e_bytes = combine_over_ranks(e0.elapsed_time(e1) / 1e3, bytes_per_step * n_e2e, world)
+
+    res = {"value": value, "unit": UNIT, "ms_per_step": ms_per_step,
+           "us_per_layer": ms_per_step * 1e3 / layers, "M": M, "layers": layers,
+           "bytes_per_step": bytes_per_step, "int_ops_per_step": ops_per_step,
+           "launches_per_step": stack.launches_per_step(fused),
+           "quantisation": "fused into the GEMV launch" if fused else "separate kernels",
+           "TFLOP/s": ops_per_step * steps * world / elapsed_max / 1e12,
+           "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                        "frac": achieved / peak, "kernel": kern, "peak_source": peak_kind,
+                        "algorithmic_per_launch": algo_per_call, "avg_launch_us": avg_launch_s * 1e6,
+                        "timing": (("timed region / product launches" if whole_step else
+                                    "graph of the product calls only, replayed like the timed region")
+                                   + "; launches overlap under programmatic dependent launch, so this is "
+                                     "step time / launches, not one kernel's duration")},
+           "e2e": {"value": e2e_bytes / e2e_el / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h},
+           "wall_s_timed": t_wall, "elapsed_s": elapsed_max}
+    return res, stack, graph, fused
+
+
+def per_shape_isolated(stack, fused, M, plan):
+    """Each product call on its own: events around each call of extra steps enqueued behind
+    a short GPU sleep (host launch overhead hidden; no overlap with the next call)."""
+    import torch
+    shapes = {name: (N, K) for name, N, K, _ in plan}
+    per_launch = {}
+    for rep in range(3):
+        evs = []
+        gpu_sleep(30.0)
+        stack.enqueue(events=evs, fused=fused)
+        torch.cuda.synchronize()
+        if rep == 0:
+            continue
+        for name, a, b in evs:
+            per_launch.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
+    return {n: {"bytes": gemv_bytes(*shapes[n], M), "us_median": statistics.median(v) * 1e6,
+                "GB/s": gemv_bytes(*shapes[n], M) / statistics.median(v) / 1e9,
+                "TFLOP/s": 2 * M * shapes[n][0] * shapes[n][1] / statistics.median(v) / 1e12}
+            for n, v in per_launch.items()}
+
+
+# The other configurations, measured in the default run (each line's own roofline and CPU
+# baseline): small steps, since each workload's graph is replayed back to back.
+OTHER_WORKLOADS = ["2b_m8", "2b_m64", "2b_m256", "8b_m1", "8b_m16", "70b_m1", "70b_m4", "70b_m16"]
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    import ternary_weight_quant_b300 as tw
+
+    model, layers, M, distinct = WORKLOADS[args.workload]
+    plan = layer_plan(model)
+    clocks = ClockSampler(local)
+    res, stack, graph, fused = measure(tw, args.workload, args.steps, args.warmup, world, args.separate,
+                                       clocks=clocks)
+    per_shape = per_shape_isolated(stack, fused, M, plan)
+    value = res["value"]
+    peak_hbm, _ = measured_peaks()
 
     # ---- default workload only: the unfused variant of the same step, the smallest case's
-    # latency per call, and a read-only streaming rate as a third bandwidth basis
+    # latency per call, a read-only streaming rate as a third bandwidth basis, and every other
+    # configuration with its own roofline and CPU baseline
     extra = {}
-    if args.workload == "2b" and not args.separate:
+    default = args.workload == "2b" and not args.separate
+    if default:
         ugraph = capture(stack, fused=False)
         for _ in range(args.warmup):
             ugraph.replay()
@@ -619,62 +710,67 @@ def run_ours(args):
         extra["us_per_layer_unfused"] = u_el / args.steps / layers * 1e6
         extra["launches_per_step_unfused"] = stack.launches_per_step(False)
         del ugraph
+    del graph, stack
+    torch.cuda.empty_cache()
+    if default:
         extra["small_case"] = small_case_latency(tw)
         extra["read_stream"] = read_stream_rate()
+    cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if default and cpu_ok:
+        extra["small_case"]["cpu_oracle_us_per_call_single_thread"] = cpu_small_case_us()
+    if default and not args.no_workloads:
+        wl = {}
+        for name in OTHER_WORKLOADS:
+            r, st, gr, _ = measure(tw, name, args.workload_steps, 3, world)
+            del st, gr
+            torch.cuda.empty_cache()
+            wmodel, wlayers, wM, wdistinct = WORKLOADS[name]
+            r["workload"] = (f"{wmodel}-shaped decoder layer, batch {wM} ({SHAPE_TEXT[wmodel]}), {wlayers} layers "
+                             f"({wdistinct} drawn, the rest byte copies in their own memory)"
+                             + ("; activations N(0,1) with 1 % outliers x20" if wmodel == "2B" else ""))
+            if cpu_ok:
+                r["cpu_baseline"] = cpu_baseline_for(wmodel, wM, args.cpu_seconds_workload,
+                                                     args.cpu_seconds_workload, outliers=(wmodel == "2B"))
+            wl[name] = r
+        extra["workloads"] = wl
 
-    # ---- CPU baseline: the oracle on the host, bounded sample (rank 0, N = 1, default workload)
+    # ---- CPU baseline: the oracle on the host, bounded sample (rank 0, N = 1)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "2b":
-        olayers = host_oracle_layers(1)
-        b, el, n = oracle_layer_sample(olayers, args.cpu_seconds, 3 * args.cpu_seconds)
-        cpu = {"value": b / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} run(s) of one 2B-shaped layer (RMSNorm/quant + 4 GEMVs, M=1), "
-                         f"single thread, {el:.1f} s; {host_cpu()}"}
+    if cpu_ok:
+        cpu = cpu_baseline_for(model, M, args.cpu_seconds, args.cpu_seconds / 2,
+                               outliers=(model == "2B" and M > 1))
 
     if rank == 0:
-        if fused:
-            kern = "tw::gemv_stream_kernel (quantisation fused)"
-        elif M <= 16:
-            kern = "tw::gemv_stream_kernel / gemv_dp4a_kernel"
-        else:
-            kern = "tw::gemm::gemm_tok_kernel / gemm_tma_kernel (tcgen05)"
-        launches = stack.launches_per_step(fused)
         workload = (WORKLOAD if args.workload == "2b" else
                     f"{model}-shaped decoder layer, batch {M} ({SHAPE_TEXT[model]}), {layers} layers "
                     f"({distinct} drawn, the rest byte copies in their own memory)")
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": workload, "M": M, "layers": layers,
-                       "bytes_per_step": bytes_per_step, "int_ops_per_step": ops_per_step,
-                       "launches_per_step": launches,
-                       "quantisation": "fused into the GEMV launch" if fused else "separate kernels",
+                       "bytes_per_step": res["bytes_per_step"], "int_ops_per_step": res["int_ops_per_step"],
+                       "launches_per_step": res["launches_per_step"],
+                       "quantisation": res["quantisation"],
                        "graph": "one CUDA graph per step",
-                       "l2": f"working set {bytes_per_step / 1e6:.0f} MB of packed weights, > 4x the 126 MB L2; "
-                             "no flush needed",
+                       "l2": f"working set {res['bytes_per_step'] / 1e6:.0f} MB of packed weights, > 4x the "
+                             "126 MB L2; no flush needed",
                        "parallelism": f"replicas x{world}"},
-            "us_per_layer": us_per_layer,
-            "TFLOP/s": ops_per_step * args.steps * world / elapsed_max / 1e12,
+            "us_per_layer": res["us_per_layer"],
+            "TFLOP/s": res["TFLOP/s"],
             "pct_of_nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
             "pct_of_measured_copy": 100.0 * value / world / peak_hbm,
             **({"pct_of_measured_read": 100.0 * value / world / extra["read_stream"]["GB/s"]}
                if "read_stream" in extra else {}),
             **extra,
-            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                         "frac": achieved / peak,
+            "roofline": {**res["roofline"],
                          "traffic": recorded_traffic(args.workload) if fused else None,
-                         "kernel": kern, "peak_source": peak_kind,
-                         "algorithmic_per_launch": algo_per_call,
-                         "avg_launch_us": avg_launch_s * 1e6,
-                         "timing": ("timed region / product launches" if whole_step else
-                                    "graph of the product calls only, replayed like the timed region"),
                          "per_shape_isolated": per_shape},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches * args.steps,
+            "e2e": res["e2e"],
+            "gpu_launches": res["launches_per_step"] * args.steps,
             "clocks": clocks.summary(),
-            "wall_s_timed": t_wall,
+            "wall_s_timed": res["wall_s_timed"],
         }
         print(json.dumps(line))
     if world > 1:
@@ -772,8 +868,14 @@ def main():
     ap.add_argument("--separate", action="store_true", help="quantisation as separate kernels")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="2b",
                     help="2b (the default decode-layer configuration), 2b_m8/m64/m256, 8b_m1/m16, 70b_m1/m4/m16")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="single-thread seconds of the CPU baseline (all cores: half of it)")
+    ap.add_argument("--cpu-seconds-workload", type=float, default=2.0,
+                    help="seconds of each CPU baseline of the other configurations (single and all-core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="default run: leave out the other configurations")
+    ap.add_argument("--workload-steps", type=int, default=10, help="timed steps of each other configuration")
     ap.add_argument("--kernel-case", default=None,
                     help="time one kernel alone: gemv, fused, fused_rms, quant, rms_quant, gemm or gemm_nows")
     ap.add_argument("--shape", default="13824x2560", help="NxK for --kernel-case")

@@ -305,8 +305,8 @@ def fused_run(tw, x, p_ref, g_ref, g=None):
 @pytest.mark.parametrize("M", [1, 2, 3, 4])
 @pytest.mark.parametrize("rms", [False, True])
 def test_quant_gemv_parity(tw, M, N, K, rms):
-    if N * K > 4_000_000 and M > 1:
-        pytest.skip("large shapes are checked at M = 1")
+    """Every shape at 1..4 tokens, with and without RMSNorm.  Above 4 M weights with more
+    than one token the oracle computes 512 sampled rows (the GPU computes all of them)."""
     W, x = si.gemv_case(M, N, K, seed=N + K + M, outliers=(M % 2 == 0))
     g = si.rms_gain(K, seed=K) if rms else None
     p_ref, g_ref = oracle.pack_ternary(W)
@@ -314,13 +314,22 @@ def test_quant_gemv_parity(tw, M, N, K, rms):
         q_ref, s_ref, sum_ref = oracle.rmsnorm_quant_act(x, g, si.RMS_EPS)
     else:
         q_ref, s_ref, sum_ref = oracle.quant_act(x)
-    y_ref, acc_ref = oracle.ternary_matmul(p_ref, g_ref, q_ref, s_ref)
-    y, acc, xq, sx, xs, y2 = fused_run(tw, x, p_ref, g_ref, g)
+    rows = np.arange(N)
+    if N * K > 4_000_000 and M > 1:
+        rows = np.sort(np.random.default_rng(N + M).choice(N, min(N, 512), replace=False))
+    y_ref, acc_ref = oracle.ternary_matmul(p_ref[rows], g_ref, q_ref, s_ref)
+    try:
+        y, acc, xq, sx, xs, y2 = fused_run(tw, x, p_ref, g_ref, g)
+    except tw.TWError as err:
+        # the documented refusal: several tokens of very long rows do not fit the fused
+        # kernel's shared memory (the separate quantisation + GEMV calls take them)
+        assert err.status == tw.TW_ERR_UNSUPPORTED and M > 1 and K >= 28672, err
+        return
     assert (xq == q_ref).all()
     assert (sx.view(np.uint32) == s_ref.view(np.uint32)).all()
     assert (xs == sum_ref).all()
-    assert (acc == acc_ref).all()
-    assert_y_close(y, y_ref)
+    assert (acc[:, rows] == acc_ref).all()
+    assert_y_close(y[:, rows], y_ref)
     assert (y2 == y).all()
     assert tw.tw_device_status() == 0
 
