@@ -30,6 +30,8 @@
 // back to the exponent-bucket histogram), so x_q is independent of launch shape.
 #include "tw_common.cuh"
 
+#include <algorithm>
+
 namespace tw {
 
 __device__ int g_stream_status;  // 0 or a tw_status recorded by a kernel (sticky until read)
@@ -603,16 +605,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
 }
 
 // ---------------------------------------------------------------------------
-// One token (the decode step): the whole weight block of a CTA copied to shared memory
-// before the dependency wait, a lean fused prologue, and per-warp row outputs.
+// One token (the decode step): the CTA's weight block copied into shared memory before
+// the dependency wait, a lean fused prologue, and per-warp row outputs.
 //
-// * Before griddepcontrol.wait one thread starts bulk copies (cp.async.bulk, completion on
-//   an mbarrier) of the CTA's rows -- contiguous in the packed tensor -- into shared
-//   memory: the weight stream of this GEMV runs while the previous kernel finishes,
-//   without holding registers.  Everything else that does not depend on the previous
-//   kernel (the RMSNorm gain, the row mapping) is also prepared before the wait.
-// * After the wait every thread loads its part of x (all loads in flight at once: one L2
-//   round trip) and stages it in shared memory.
+// * A CTA owns a contiguous block of rows (contiguous in the packed tensor); one thread
+//   copies all of it into shared memory with cp.async.bulk (completion on an mbarrier)
+//   before griddepcontrol.wait, so the weight stream of this GEMV runs while the previous
+//   kernel finishes, without holding registers.  Everything else that does not depend on
+//   the previous kernel (the RMSNorm gain, the row mapping) is also prepared before the
+//   wait.  Used when the block fits (a 2B-shaped layer, 8B q|k|v and o); longer streams
+//   take gemv_stream_kernel.  The kernel is kept small: its code is fetched afresh after
+//   every dependency wait, and a larger body measurably lengthened that wait.
+// * After the wait every thread loads its NV float4s of x (all loads in flight at once:
+//   one L2 round trip).
 // * Pass 1 (registers only): per warp either the largest |x| (no RMSNorm: that is a) or,
 //   with RMSNorm, the float-float sum of squares and the float4 holding the largest
 //   p = fl(|x| |g|).  After the first barrier every warp combines the per-warp results
@@ -632,9 +637,10 @@ constexpr int kDecThreads = kDecWarps * 32;
 struct DecodeRed {
   float2 ff[kDecWarps];   // per-warp float-float sums of squares
   uint32_t pm[kDecWarps]; // per-warp largest p (RMSNorm) or |x|, as bits
-  int pi[kDecWarps];      // float4 index of that p
+  float4 cx[kDecWarps];   // per-warp candidate float4 of x ...
+  float4 cg[kDecWarps];   // ... and of the gain
   uint32_t am[kDecWarps]; // re-check: per-warp largest |u|
-  int qs[kDecWarps];      // per-warp sums of x_q (CTA 0, when asked)
+  int qs[kDecWarps];      // per-warp sums of x_q
   int viol;               // some |u_k| exceeded the candidate scale
 };
 
@@ -664,18 +670,17 @@ __device__ __forceinline__ bool dec_mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Quantises this thread's NV float4s of x (registers: xv, and the gain gv when RMS) with
-// scale amax into xs; float4 q of the thread is unit tid + q * kDecThreads.  Returns the
-// thread's sum of x_q; sets *viol when `check` and some |u| > amax.
+// The unit (float4 index of x) of this thread's float4 q.
+__device__ __forceinline__ int dec_unit(int q) { return q * kDecThreads + (int)threadIdx.x; }
+
+// Quantises this thread's float4s of x (registers xv, and the gain gv when RMS) with scale
+// amax into xs.  Returns the thread's sum of x_q; sets *viol when `check` and some |u| > amax.
 template <bool RMS, int NV>
 __device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, const float4 (&xv)[NV],
-                                               const float4 (&gv)[NV], float inv, float amax, bool check,
-                                               int* viol) {
-  const int tid = threadIdx.x;
+                                               const float4 (&gv)[NV], float inv, float amax, float ra,
+                                               bool check, int* viol) {
   const int K4 = a.K >> 2;
   unsigned char* xsb = reinterpret_cast<unsigned char*>(xs);
-  float ra = amax == 0.0f ? 0.0f : __int_as_float(0x7fffffff);
-  if (amax >= 0x1p-120f && amax <= 0x1p120f) asm("rcp.approx.f32 %0, %1;" : "=f"(ra) : "f"(amax));
   // d = fl(fl(u 127) ra) is within 2^-22 |d| < 3.1e-5 of fl(u 127) / a (|d| <= 127 once
   // |u| <= a); when it is at least 5e-5 from a half-integer, rounding d gives
   // round_half_even(fl32(fl(u 127) / a)).  Rounding by adding 1.5 2^23: the integer is then
@@ -686,7 +691,7 @@ __device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, c
   bool any = false, bad = false;
 #pragma unroll
   for (int q = 0; q < NV; ++q) {
-    const bool valid = tid + q * kDecThreads < K4;
+    const bool valid = dec_unit(q) < K4;
     float4 v = valid ? xv[q] : make_float4(0.f, 0.f, 0.f, 0.f);
     if (RMS) {
       const float4 gg = gv[q];
@@ -728,7 +733,7 @@ __device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, c
   int qsum = 0;
 #pragma unroll
   for (int q = 0; q < NV; ++q) {
-    const int u = tid + q * kDecThreads;
+    const int u = dec_unit(q);
     if (u < K4) {
       qsum = __dp4a((int)pq[q], 0x01010101, qsum);
       if (blockIdx.x == 0 && a.x_q_out) reinterpret_cast<uint32_t*>(a.x_q_out)[u] = pq[q];
@@ -746,51 +751,46 @@ __device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, c
 
 // The one-token prologue: x (fp32, global) -> xs (byte-transposed int8 groups).  Returns
 // a = max |u|; sets *cs to the dequantisation scale fl(fl(gamma a) / 127) and *xtot to the
-// sum of x_q over the whole row.  A thread holds float4s tid + q * kDecThreads (q < NV,
-// NV * kDecThreads >= K/4) of x, and of the gain in gv (RMS; loaded before the dependency
-// wait).  xf4 is the staging area for x ([K/4] float4), followed by the staged gain.
+// sum of x_q over the whole row.  A thread's float4s are units dec_unit(q), q < NV
+// (NV * kDecThreads >= K / 4); gv holds the gain's (RMS: loaded before the dependency wait).
 template <bool RMS, int NV>
-__device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs, float4* xf4, const float4 (&gv)[NV],
-                                                 DecodeRed& r, uint32_t* red_u, unsigned long long* red_lo,
+__device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs, float4 (&gv)[NV], DecodeRed& r,
+                                                 uint32_t* red_u, unsigned long long* red_lo,
                                                  unsigned long long* red_hi, uint32_t (*limb)[256],
                                                  unsigned long long* hist, double* s_dbl, float* s_inv,
                                                  int* s_slow, float gam, float* cs, int* xtot) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned full = 0xffffffffu;
   const int K = a.K, K4 = K >> 2;
-  const float4* g4 = xf4 + K4;
   const float4* xg = reinterpret_cast<const float4*>(a.x);
-
-  // ---- x: this thread's loads all in flight, then staged for the other warps
   float4 xv[NV];
 #pragma unroll
-  for (int q = 0; q < NV; ++q)
-    xv[q] = tid + q * kDecThreads < K4 ? __ldcg(xg + tid + q * kDecThreads) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int q = 0; q < NV; ++q)
-    if (tid + q * kDecThreads < K4) xf4[tid + q * kDecThreads] = xv[q];
+  for (int q = 0; q < NV; ++q) xv[q] = dec_unit(q) < K4 ? __ldcg(xg + dec_unit(q)) : make_float4(0.f, 0.f, 0.f, 0.f);
 
   // ---- pass 1 (padding float4s are zero: they add nothing)
   FF s0 = {0.0f, 0.0f}, s1 = {0.0f, 0.0f}, s2 = {0.0f, 0.0f}, s3 = {0.0f, 0.0f};
   float pmf = 0.0f;
-  int pi = 0;
+  float4 cxv = make_float4(0.f, 0.f, 0.f, 0.f), cgv = cxv;
+  {
 #pragma unroll
-  for (int q = 0; q < NV; ++q) {
-    const float4 v = xv[q];
-    if (RMS) {
-      const float4 gg = gv[q];
-      ff_add_square(s0, v.x);  // one chain per component
-      ff_add_square(s1, v.y);
-      ff_add_square(s2, v.z);
-      ff_add_square(s3, v.w);
-      const float m = fmaxf(fmaxf(fabsf(__fmul_rn(v.x, gg.x)), fabsf(__fmul_rn(v.y, gg.y))),
-                            fmaxf(fabsf(__fmul_rn(v.z, gg.z)), fabsf(__fmul_rn(v.w, gg.w))));
-      if (m > pmf) {
-        pmf = m;
-        pi = tid + q * kDecThreads;
+    for (int q = 0; q < NV; ++q) {
+      const float4 v = xv[q];
+      if (RMS) {
+        const float4 gg = gv[q];
+        ff_add_square(s0, v.x);  // one chain per component
+        ff_add_square(s1, v.y);
+        ff_add_square(s2, v.z);
+        ff_add_square(s3, v.w);
+        const float m = fmaxf(fmaxf(fabsf(__fmul_rn(v.x, gg.x)), fabsf(__fmul_rn(v.y, gg.y))),
+                              fmaxf(fabsf(__fmul_rn(v.z, gg.z)), fabsf(__fmul_rn(v.w, gg.w))));
+        if (m > pmf) {
+          pmf = m;
+          cxv = v;
+          cgv = gg;
+        }
+      } else {
+        pmf = fmaxf(pmf, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
       }
-    } else {
-      pmf = fmaxf(pmf, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
   }
   const uint32_t pm = __float_as_uint(pmf);  // >= 0: compares as its bits
@@ -806,15 +806,15 @@ __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs,
       t.lo = __shfl_xor_sync(full, s0.lo, o);
       ff_add(s0, t);
     }
-    const int wi = __shfl_sync(full, pi, __ffs(__ballot_sync(full, pm == wm)) - 1);
-    if (lane == 0) {
-      r.ff[warp] = make_float2(s0.hi, s0.lo);
-      r.pi[warp] = wi;
+    if (lane == __ffs(__ballot_sync(full, pm == wm)) - 1) {
+      r.cx[warp] = cxv;
+      r.cg[warp] = cgv;
     }
+    if (lane == 0) r.ff[warp] = make_float2(s0.hi, s0.lo);
   }
   if (lane == 0) r.pm[warp] = wm;
   if (tid == 0) r.viol = 0;
-  __syncthreads();  // (1) per-warp results and the staged copy of x
+  __syncthreads();  // (1) per-warp results
 
   // ---- every warp: combine (kDecWarps <= 16 partials, one per lane)
   const uint32_t ml = lane < kDecWarps ? r.pm[lane] : 0u;
@@ -842,23 +842,27 @@ __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs,
     float ms = 0.0f;
     if (ff_mean_f32(t, K, a.inv_k, ms)) {
       inv = inv_rms_f32(ms, a.eps);
-    } else {  // block-uniform
-      inv = rms_inv_exact<kDecWarps>(xf4, K4, a.kd, a.eps, red_u, red_lo, red_hi, limb, hist, s_dbl, s_inv, s_slow);
+    } else {  // block-uniform; reads x again (from L2)
+      inv = rms_inv_exact<kDecWarps>(xg, K4, a.kd, a.eps, red_u, red_lo, red_hi, limb, hist, s_dbl, s_inv, s_slow);
     }
-    const int pil = lane < kDecWarps ? r.pi[lane] : 0;
-    const int ks = __shfl_sync(full, pil, __ffs(__ballot_sync(full, lane < kDecWarps && ml == bm)) - 1);
-    const float4 v = xf4[ks], gg = g4[ks];
+    const int wsel = __ffs(__ballot_sync(full, lane < kDecWarps && ml == bm)) - 1;
+    const float4 v = r.cx[wsel], gg = r.cg[wsel];
     amax = fmaxf(fmaxf(fabsf(__fmul_rn(__fmul_rn(v.x, inv), gg.x)), fabsf(__fmul_rn(__fmul_rn(v.y, inv), gg.y))),
                  fmaxf(fabsf(__fmul_rn(__fmul_rn(v.z, inv), gg.z)), fabsf(__fmul_rn(__fmul_rn(v.w, inv), gg.w))));
   }
   *cs = dequant_scale(gam, amax);
 
-  // ---- quantisation (with RMSNorm: checks the candidate scale)
-  int qsum = decode_quantise<RMS, NV>(a, xs, xv, gv, inv, amax, RMS, &r.viol);
-  qsum = __reduce_add_sync(full, qsum);
-  if (lane == 0) r.qs[warp] = qsum;
-  __syncthreads();  // (2) xs and the per-warp sums complete; r.viol final
-  if (RMS && r.viol) {  // block-uniform, rare: a from all elements, then quantise again
+  // ---- quantisation.  With RMSNorm the first pass checks the candidate scale; when some
+  // |u| exceeded it (block-uniform, rare) a is taken over all elements and the same code
+  // quantises once more.
+  for (int pass = 0;; ++pass) {
+    float ra = amax == 0.0f ? 0.0f : __int_as_float(0x7fffffff);
+    if (amax >= 0x1p-120f && amax <= 0x1p120f) asm("rcp.approx.f32 %0, %1;" : "=f"(ra) : "f"(amax));
+    int qs = decode_quantise<RMS, NV>(a, xs, xv, gv, inv, amax, ra, RMS && pass == 0, &r.viol);
+    qs = __reduce_add_sync(full, qs);
+    if (lane == 0) r.qs[warp] = qs;
+    __syncthreads();  // (2) xs and the per-warp sums complete; r.viol final
+    if (!RMS || pass > 0 || !r.viol) break;
     float m = 0.0f;
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
@@ -868,14 +872,9 @@ __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs,
     }
     const uint32_t am = __reduce_max_sync(full, __float_as_uint(m));
     if (lane == 0) r.am[warp] = am;
-    __syncthreads();
+    __syncthreads();  // also: every warp has read r.qs of the first pass
     amax = __uint_as_float(__reduce_max_sync(full, lane < kDecWarps ? r.am[lane] : 0u));
     *cs = dequant_scale(gam, amax);
-    qsum = decode_quantise<RMS, NV>(a, xs, xv, gv, inv, amax, false, &r.viol);
-    qsum = __reduce_add_sync(full, qsum);
-    __syncthreads();  // every warp has read r.am and r.qs
-    if (lane == 0) r.qs[warp] = qsum;
-    __syncthreads();
   }
   *xtot = __reduce_add_sync(full, lane < kDecWarps ? r.qs[lane] : 0);
   if (blockIdx.x == 0 && tid == 0) {
@@ -885,9 +884,9 @@ __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs,
   return amax;
 }
 
-// R rows of one warp (rows i0 .. i0+R-1 of its group): per-lane partial dot products from
-// the shared-memory copy of the weights, then one warp sum per row.  Words of the lane's
-// range past its K slice meet x = 0 there, so their (arbitrary) weights add nothing.
+// R rows of one warp (rows i0 .. i0+R-1 of its group, in the chunk at wsm): per-lane partial
+// dot products from shared memory, then one warp sum per row.  Words of the lane's range
+// past its K slice meet x = 0 there, so their (arbitrary) weights add nothing.
 template <int JMAX, int R>
 __device__ __forceinline__ void decode_rows(const uint32_t* wsm, int Kw, int G, int gr, int i0, int wbase,
                                             const uint4 (&xr)[JMAX], int (&tot)[4]) {
@@ -913,8 +912,8 @@ __device__ __forceinline__ void decode_rows(const uint32_t* wsm, int Kw, int G, 
 }
 
 // The fused one-token GEMV (see above).  Dynamic shared memory: the CTA's packed rows at
-// offset 0 (then slack for the last row's reads past its slice), xs (a.xs_off), the staged
-// x and gain (a.xf_off), the row totals (a.acc_off, used when S > 1).
+// offset 0 (plus slack for the last row's reads past its slice), xs (a.xs_off), the row
+// totals (a.acc_off, used when S > 1).
 template <int JMAX, int NV, bool RMS>
 __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -923,10 +922,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
   const int c = blockIdx.x;
   const int nrows = a.rows_base + (c < a.rows_rem ? 1 : 0);
   const int row0 = c * a.rows_base + min(c, a.rows_rem);
-  const uint32_t* wsm = reinterpret_cast<const uint32_t*>(smem);          // [nrows][Kw] packed words
-  uint4* xs = reinterpret_cast<uint4*>(smem + a.xs_off);                 // [Kw] byte-transposed x_q
-  float4* xf4 = reinterpret_cast<float4*>(smem + a.xf_off);              // x [K/4] (+ gain [K/4])
-  int* sacc = reinterpret_cast<int*>(smem + a.acc_off);                  // [nrows] (S > 1)
+  const uint32_t* wsm = reinterpret_cast<const uint32_t*>(smem);  // [nrows][Kw] packed words
+  uint4* xs = reinterpret_cast<uint4*>(smem + a.xs_off);         // [Kw] byte-transposed x_q
+  int* sacc = reinterpret_cast<int*>(smem + a.acc_off);          // [nrows] (S > 1)
   __shared__ DecodeRed red;
   __shared__ __align__(8) unsigned long long wbar;
   __shared__ uint32_t red_u[RMS ? kDecWarps : 1];
@@ -947,9 +945,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
     const uint32_t total = (uint32_t)nrows * (uint32_t)(K >> 2);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(total) : "memory");
     const unsigned char* src = a.packed + (size_t)row0 * (K >> 2);
-    constexpr uint32_t kChunk = 16384;
-    for (uint32_t off = 0; off < total; off += kChunk) {
-      const uint32_t n = min(kChunk, total - off);
+    for (uint32_t off = 0; off < total; off += 32768u) {
+      const uint32_t n = min(32768u, total - off);
       asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                        smem_addr(smem + off)),
                    "l"(src + off), "r"(n), "r"(bar)
@@ -960,16 +957,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
   const int S = a.S, G = kDecWarps / S;
   if (S > 1)
     for (int i = tid; i < nrows; i += kDecThreads) sacc[i] = 0;
-  float4 gv[NV];  // this thread's float4s of the RMSNorm gain (also staged for the other warps)
+  float4 gv[NV];  // this thread's float4s of the RMSNorm gain
 #pragma unroll
   for (int q = 0; q < NV; ++q) {
-    gv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (RMS && tid + q * kDecThreads < (K >> 2)) {
-      gv[q] = __ldg(reinterpret_cast<const float4*>(a.g) + tid + q * kDecThreads);
-      xf4[(K >> 2) + tid + q * kDecThreads] = gv[q];
-    }
+    const int u = dec_unit(q);
+    gv[q] = (RMS && u < (K >> 2)) ? __ldg(reinterpret_cast<const float4*>(a.g) + u) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  // the rows and K slice of this warp
+  // the rows and K slice of this warp (integer divisions are slow here: before the wait)
   const int sl = warp % S, gr = warp / S;
   const int Ws = (Kw + S - 1) / S;
   const int ws0 = sl * Ws, ws1 = min(Kw, ws0 + Ws);
@@ -981,7 +975,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
 
   float cs;
   int xtot;
-  const float amax = decode_prologue<RMS, NV>(a, xs, xf4, gv, red, red_u, red_lo, red_hi, limb, hist, &s_dbl, s_inv,
+  const float amax = decode_prologue<RMS, NV>(a, xs, gv, red, red_u, red_lo, red_hi, limb, hist, &s_dbl, s_inv,
                                               s_slow, gam, &cs, &xtot);
   const bool cs_normal = cs >= 1.17549435e-38f;
 
@@ -996,39 +990,34 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
   // up only as a whole
   const bool arrived = __all_sync(0xffffffffu, dec_mbar_wait(bar, 0));
   if (!arrived && lane == 0) atomicCAS(&g_stream_status, 0, (int)TW_ERR_TIMEOUT);
-
-  auto emit = [&](int i0, int n, const int (&tot)[4]) {
-    if (lane == 0) {
+  if (arrived) {
+    auto emit = [&](int i0, int n, const int (&tot)[4]) {
+      if (lane == 0) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q < n) {
-          const int rr = gr + (i0 + q) * G;
-          if (S == 1) {
-            const int acc = tot[q] - xtot;
-            a.y[row0 + rr] = cs_normal ? __fmul_rn((float)acc, cs) : dequant_tiny(acc, gam, amax);
-            if (a.acc_out) a.acc_out[row0 + rr] = acc;
-          } else {
-            atomicAdd(&sacc[rr], tot[q]);
+        for (int q = 0; q < 4; ++q) {
+          if (q < n) {
+            const int rr = gr + (i0 + q) * G;  // row within the CTA
+            if (S == 1) {
+              const int acc = tot[q] - xtot;
+              a.y[row0 + rr] = cs_normal ? __fmul_rn((float)acc, cs) : dequant_tiny(acc, gam, amax);
+              if (a.acc_out) a.acc_out[row0 + rr] = acc;
+            } else {
+              atomicAdd(&sacc[rr], tot[q]);
+            }
           }
         }
       }
-    }
-  };
-  if (arrived) {
+    };
+    // RB rows at a time (independent chains) while that many remain, then one by one
+    constexpr int RB = JMAX <= 5 ? 4 : 2;
     const int wbase = ws0 + lane;
     int i0 = 0;
     int tot[4];
-    if constexpr (JMAX <= 5) {  // four rows at a time while registers allow
-      for (; i0 + 4 <= nr; i0 += 4) {
-        decode_rows<JMAX, 4>(wsm, Kw, G, gr, i0, wbase, xr, tot);
-        emit(i0, 4, tot);
-      }
+    for (; i0 + RB <= nr; i0 += RB) {
+      decode_rows<JMAX, RB>(wsm, Kw, G, gr, i0, wbase, xr, tot);
+      emit(i0, RB, tot);
     }
-    for (; i0 + 2 <= nr; i0 += 2) {
-      decode_rows<JMAX, 2>(wsm, Kw, G, gr, i0, wbase, xr, tot);
-      emit(i0, 2, tot);
-    }
-    if (i0 < nr) {
+    for (; i0 < nr; ++i0) {
       decode_rows<JMAX, 1>(wsm, Kw, G, gr, i0, wbase, xr, tot);
       emit(i0, 1, tot);
     }
@@ -1042,8 +1031,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
       }
     }
   }
-  // a CTA that gave up leaves its outputs unwritten, but must not exit while its copies
-  // may still land in shared memory: one more bounded wait
+  // a warp that gave up must not let the CTA exit while the copy may still land in shared
+  // memory: one more bounded wait
   if (!arrived) dec_mbar_wait(bar, 0);
 }
 
@@ -1115,8 +1104,6 @@ cudaError_t launch(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, 
   auto kern = tw::gemv_stream_kernel<MT, JMAX, pre_for(MT, JMAX), FUSED, RMS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);
   cfg.blockDim = dim3(tw::kThreads);
@@ -1131,10 +1118,11 @@ cudaError_t launch(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, 
 }
 
 // Launch plan of the one-token decode kernel: one CTA per SM (the other slot is left to the
-// next launch), the CTA's packed rows, x_q, the staged x (and gain) and the row totals in
-// dynamic shared memory.  False when that does not fit in kDecodeSmemMax.
+// next launch); the CTA's packed rows, x_q and the row totals in dynamic shared memory, at
+// most kDecodeSmemMax bytes, and x in at most 4 (with RMSNorm) or 8 float4s per thread.  False otherwise
+// (the caller then takes gemv_stream_kernel).
 bool make_decode_plan(int N, int K, int num_sms, bool rms, Plan& p) {
-  if (K % 64 != 0 || K > 16384) return false;
+  if (K % 64 != 0 || K / 4 > (rms ? 4 : 8) * tw::kDecThreads) return false;
   const int Kw = K / 16;
   p.S = 0;
   for (int S : {1, 2, 4, 8, 16}) {  // divisors of the decode kernel's warp count
@@ -1151,16 +1139,12 @@ bool make_decode_plan(int N, int K, int num_sms, bool rms, Plan& p) {
   p.rows_rem = N % p.grid;
   const size_t max_rows = (size_t)p.rows_base + (p.rows_rem ? 1 : 0);
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
-  // the last row's lanes read up to S * 32 * jmax - Kw words past its end (against x = 0)
+  // the last row has lanes reading up to S * 32 * jmax - Kw words past its end (against x = 0)
   const size_t slack = (size_t)(p.S * 32 * p.jmax - Kw) * 4;
-  size_t off = up(max_rows * (size_t)(K / 4) + slack, 128);
-  p.xs_off = (int)off;
-  off = up(off + (size_t)K, 16);
-  p.xf_off = (int)off;
-  off += (size_t)(rms ? 2 : 1) * K * 4;
-  p.acc_off = (int)off;
-  off += p.S > 1 ? up(max_rows * 4, 16) : 0;
-  p.smem = off;
+  p.xs_off = (int)up(max_rows * (size_t)(K / 4) + slack, 128);
+  p.acc_off = p.xs_off + (int)up((size_t)K, 16);
+  p.xf_off = -1;
+  p.smem = (size_t)p.acc_off + (p.S > 1 ? up(max_rows * 4, 16) : 0);
   return p.smem <= kDecodeSmemMax;
 }
 
@@ -1187,8 +1171,8 @@ cudaError_t launch_decode(const tw::StreamArgs& a, const Plan& p, cudaStream_t s
 }
 
 // The kernel's template arguments follow from the plan: JMAX = words per lane and row, NV =
-// float4s of x per thread, ceil(K / 4 / kDecThreads): 2 when one warp spans K (S = 1), up to 4
-// with two K slices, up to 8 with four (the plan admits K <= 16384).
+// float4s of x per thread, ceil(K / 4 / kDecThreads) rounded up to 2, 4 or 8 (2 when one warp
+// spans K, S = 1; up to 4 with two K slices; 8, without RMSNorm only, with four).
 template <bool RMS>
 cudaError_t dispatch_decode(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, bool pdl) {
   const int nv = (a.K / 4 + tw::kDecThreads - 1) / tw::kDecThreads;
@@ -1212,7 +1196,7 @@ cudaError_t dispatch_decode(const tw::StreamArgs& a, const Plan& p, cudaStream_t
       case 8: return launch_decode<8, 4, RMS>(a, p, stream, pdl);
       default: break;
     }
-  } else if (nv <= 8) {
+  } else if constexpr (!RMS) {
     switch (p.jmax) {
       case 5: return launch_decode<5, 8, RMS>(a, p, stream, pdl);
       case 6: return launch_decode<6, 8, RMS>(a, p, stream, pdl);
@@ -1283,7 +1267,8 @@ cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, cons
   a.x_q_out = x_q_out; a.s_x_out = s_x_out; a.x_sum_out = x_sum_out;
   fill_plan(a, p);
   Plan dp;
-  if (M == 1 && make_decode_plan(N, K, num_sms, g != nullptr, dp)) {  // one token: the decode kernel
+  // one token whose CTA weight block fits in shared memory: the decode kernel
+  if (M == 1 && make_decode_plan(N, K, num_sms, g != nullptr, dp)) {
     fill_plan(a, dp);
     return g ? dispatch_decode<true>(a, dp, stream, pdl) : dispatch_decode<false>(a, dp, stream, pdl);
   }
