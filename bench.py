@@ -782,7 +782,7 @@ def run_ours(args):
 def run_kernel_case(args):
     """Kernels in isolation (for timing sweeps and small ncu captures; not the contract line).
 
-    --kernel-case {gemv,fused,fused_rms,quant,rms_quant,gemm,gemm_nows} (a comma list) on --shape
+    --kernel-case {gemv,fused,fused_rms,quant,rms_quant,gemm,gemm_nows,matmul} (a comma list) on --shape
     NxK at --M tokens (a comma list), over --copies distinct weight tensors (so the stream leaves
     L2); one pass over them is captured in a CUDA graph and replayed --reps times (device time
     per launch, host launch cost excluded).  One JSON line per (case, M)."""
@@ -821,6 +821,8 @@ def run_kernel_case(args):
                     tw.tw_ternary_gemm(p, g, xq, sx, y, workspace=gws)
                 elif k == "gemm_nows":
                     tw.tw_ternary_gemm(p, g, xq, sx, y)
+                elif k == "matmul":
+                    tw.tw_ternary_matmul(p, g, xq, sx, y, xs, workspace=gws)
                 else:
                     raise SystemExit(f"unknown kernel case {k}")
 
@@ -877,7 +879,7 @@ def main():
                     help="default run: leave out the other configurations")
     ap.add_argument("--workload-steps", type=int, default=10, help="timed steps of each other configuration")
     ap.add_argument("--kernel-case", default=None,
-                    help="time one kernel alone: gemv, fused, fused_rms, quant, rms_quant, gemm or gemm_nows")
+                    help="time one kernel alone: gemv, fused, fused_rms, quant, rms_quant, gemm, gemm_nows or matmul")
     ap.add_argument("--shape", default="13824x2560", help="NxK for --kernel-case")
     ap.add_argument("--M", default="1", help="tokens for --kernel-case (a comma list)")
     ap.add_argument("--copies", type=int, default=8, help="distinct weight tensors for --kernel-case")

@@ -39,6 +39,15 @@
  *   - All data pointers are DEVICE pointers owned by the caller (cudaMalloc'd or
  *     managed memory); the library allocates nothing and never synchronises
  *     (tw_device_status excepted).
+ *   - The quantisation and product calls are launched with programmatic dependent
+ *     launch: a kernel of this library may start while the kernel enqueued just before
+ *     it on `stream` is still running, if that kernel lets its dependents start early
+ *     (griddepcontrol.launch_dependents: this library's quantisation and product
+ *     kernels do; its packing kernels and ordinary kernels do not).  Before that kernel
+ *     has finished it reads only its parameters -- the packed weights, w_scale and the
+ *     RMSNorm gain -- never the activations, and writes nothing.  So do not let the
+ *     kernel just before a product call write that call's weights, scale or gain while
+ *     allowing early starts (weights packed at load time are always fine).
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and runs
  *     asynchronously; results are valid once the stream reaches that point.
  *   - Arguments are checked on the host before anything is enqueued: a failed
@@ -172,8 +181,11 @@ TW_API tw_status tw_rmsnorm_quant_act(const float *x, const float *g, float eps,
  *   y        [M][N] fp32 output.
  *   acc_out  [M][N] int32 output of the exact accumulators, or NULL.
  * Requires 1 <= M <= TW_GEMV_MAX_M, N >= 1, 4 <= K <= TW_MAX_K, K % 4 == 0.  The fast
- * paths need K % 16 == 0 (K % 64 == 0 for the shared-memory streaming kernel),
- * packed and x_q 16-byte aligned; other cases take a slower exact path.
+ * paths need K % 64 == 0 and packed and x_q 16-byte aligned: up to 4 tokens the
+ * streaming kernel (integer dp4a), from 5 to 16 the tensor cores through mma.sync with
+ * f16 operands and fp32 accumulation, exact (the 2-bit codes enter as f16 bit patterns
+ * c 4^s 2^-24, the activations scaled by 4^-s; every partial sum is a multiple of
+ * 2^-24 below 1).  Other cases take a slower exact path (dp4a).
  */
 TW_API tw_status tw_ternary_gemv(const uint8_t *packed, const float *w_scale, const int8_t *x_q,
                                  const float *s_x, const int32_t *x_sum, int64_t M, int64_t N,
@@ -244,7 +256,8 @@ TW_API tw_status tw_ternary_gemm(const uint8_t *packed, const float *w_scale, co
 
 /*
  * The product for any M: tw_ternary_gemv below the measured crossover (M <= 16; M <= 11
- * for matrices of 2^24 weights or more when a large enough workspace is given, K % 64 == 0),
+ * for matrices of 2^24 weights or more with K >= 4096 when a large enough workspace is
+ * given, K % 64 == 0),
  * tw_ternary_gemm above it (when K % 16 == 0 and packed / x_q are 16-byte aligned; an
  * exact CUDA-core kernel otherwise).  Arguments as tw_ternary_gemm; the workspace is
  * used only on the tensor-core path and may be NULL.

@@ -117,6 +117,11 @@ __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict_
   __shared__ unsigned long long red_lo[32], red_hi[32];
   __shared__ float sh_inv;
 
+  // programmatic dependent launch: the next kernel may start its own preparation now; x may
+  // come from the previous kernel, so it is read only after that kernel has finished
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   // first pass
   uint32_t mx = 0u;
   FF s0 = {0.0f, 0.0f}, s1 = {0.0f, 0.0f}, s2 = {0.0f, 0.0f}, s3 = {0.0f, 0.0f};
@@ -262,15 +267,29 @@ static int act_threads(long long K) {
   return t;
 }
 
+// Launched with programmatic dependent launch (the kernel waits before reading x).
+template <bool RMS>
+static cudaError_t launch_act(const float* x, const float* g, float eps, long long M, long long K, int8_t* x_q,
+                              float* s_x, int32_t* x_sum, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)M);
+  cfg.blockDim = dim3((unsigned)act_threads(K));
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tw::act_quant_kernel<RMS>, x, g, eps, (int)K, tw::make_kdiv((int)K),
+                            1.0f / (float)K, x_q, s_x, x_sum);
+}
+
 cudaError_t tw_launch_quant_act(const float* x, long long M, long long K, int8_t* x_q, float* s_x,
                                 int32_t* x_sum, cudaStream_t stream) {
-  tw::act_quant_kernel<false><<<(unsigned)M, act_threads(K), 0, stream>>>(x, nullptr, 0.0f, (int)K, tw::make_kdiv((int)K), 1.0f / (float)K, x_q, s_x,
-                                                                         x_sum);
-  return cudaGetLastError();
+  return launch_act<false>(x, nullptr, 0.0f, M, K, x_q, s_x, x_sum, stream);
 }
 
 cudaError_t tw_launch_rmsnorm_quant_act(const float* x, const float* g, float eps, long long M, long long K,
                                         int8_t* x_q, float* s_x, int32_t* x_sum, cudaStream_t stream) {
-  tw::act_quant_kernel<true><<<(unsigned)M, act_threads(K), 0, stream>>>(x, g, eps, (int)K, tw::make_kdiv((int)K), 1.0f / (float)K, x_q, s_x, x_sum);
-  return cudaGetLastError();
+  return launch_act<true>(x, g, eps, M, K, x_q, s_x, x_sum, stream);
 }

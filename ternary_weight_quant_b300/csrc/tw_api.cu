@@ -36,7 +36,12 @@ cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, cons
                                  float* s_x_out, int32_t* x_sum_out, int32_t* acc_out, cudaStream_t stream,
                                  int num_sms, bool pdl);
 cudaError_t tw_read_stream_status(int* out);
+int tw_mma_supported(int M, int N, int K);
+cudaError_t tw_launch_gemv_mma(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
+                               int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream,
+                               int num_sms);
 cudaError_t tw_read_gemm_status(int* out);
+cudaError_t tw_read_mma_status(int* out);
 cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
                            int M, int N, int K, float* y, int32_t* acc_out, void* workspace, cudaStream_t stream,
                            int num_sms, int* unsupported);
@@ -112,6 +117,10 @@ tw_status check_product_args(const uint8_t* packed, const float* w_scale, const 
 }
 
 }  // namespace
+
+// Tokens from which tw_ternary_gemv takes the tensor-core (mma.sync) kernel (up to 16): below
+// it the integer product of the streaming kernel is cheaper than an 8-token tensor tile.
+static const int64_t kMmaMinM = 5;
 
 extern "C" {
 
@@ -210,9 +219,12 @@ TW_API tw_status tw_ternary_gemv(const uint8_t* packed, const float* w_scale, co
   if (st != TW_OK) return st;
   st = check_device_ptrs(packed, w_scale, x_q, s_x, x_sum, y, acc_out);
   if (st != TW_OK) return st;
+  if (M >= kMmaMinM && aligned(packed, 16) && aligned(x_q, 16) && tw_mma_supported((int)M, (int)N, (int)K))
+    return from_cuda(tw_launch_gemv_mma(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
+                                        (cudaStream_t)stream, sms));
   if (aligned(packed, 16) && aligned(x_q, 16) && tw_stream_supported((int)M, (int)N, (int)K, sms))
     return from_cuda(tw_launch_gemv_stream(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
-                                           (cudaStream_t)stream, sms, false));
+                                           (cudaStream_t)stream, sms, true));
   return from_cuda(tw_launch_gemv(packed, w_scale, x_q, s_x, x_sum, (int)M, (int)N, (int)K, y, acc_out,
                                   (cudaStream_t)stream));
 }
@@ -264,19 +276,19 @@ TW_API tw_status tw_ternary_gemm(const uint8_t* packed, const float* w_scale, co
   return from_cuda(e);
 }
 
-// Token count from which the tensor-core GEMM takes over from the GEMV kernels.  Between 9
-// and 16 tokens the dp4a GEMV's cost grows with M while the tokens-on-M GEMM's stays flat, so
-// for large matrices (N K >= 2^24, e.g. 13824 x 2560 or 2560 x 6912) the GEMM takes over at 12
-// tokens when it can use its workspace (measured on B300: at 12 tokens 2560 x 6912 takes
-// 21.1 us as a GEMV and 14.6 us as a GEMM; 3840 x 2560 stays faster as a GEMV up to 16).
+// Token count from which the tcgen05 GEMM takes over from the GEMV kernels (the mma.sync
+// kernel from 5 to 16 tokens).  Measured on B300, microseconds per call chained in a graph:
+// 13824 x 2560 at 16 tokens 11.3 (mma.sync) against 18.0 (GEMM); 2560 x 6912 at 16 tokens
+// 18.9 against 14.7, and at 8 tokens 12.5 against 14.4.  So long rows (K >= 4096) of large
+// matrices (N K >= 2^24) go to the GEMM from 12 tokens when it can use its workspace.
 static const int64_t kGemmCrossoverM = 17;
 static const int64_t kGemmCrossoverLargeM = 12;
 static const int64_t kLargeWeights = (int64_t)1 << 24;
 
 static bool prefer_gemm(int64_t M, int64_t N, int64_t K, const void* workspace, size_t ws_bytes) {
   if (M >= kGemmCrossoverM || M > TW_GEMV_MAX_M) return true;
-  return M >= kGemmCrossoverLargeM && N * K >= kLargeWeights && K % 64 == 0 && workspace != nullptr &&
-         ws_bytes >= tw_gemm_ws_size((int)M, (int)K);
+  return M >= kGemmCrossoverLargeM && K >= 4096 && N * K >= kLargeWeights && K % 64 == 0 &&
+         workspace != nullptr && ws_bytes >= tw_gemm_ws_size((int)M, (int)K);
 }
 
 TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, const int8_t* x_q,
@@ -303,12 +315,13 @@ TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, 
 
 TW_API tw_status tw_device_status(int32_t* status) {
   if (!status) return TW_ERR_NULL;
-  int v = 0, g = 0;
-  if (tw_read_stream_status(&v) != cudaSuccess || tw_read_gemm_status(&g) != cudaSuccess) {
+  int v = 0, g = 0, m = 0;
+  if (tw_read_stream_status(&v) != cudaSuccess || tw_read_gemm_status(&g) != cudaSuccess ||
+      tw_read_mma_status(&m) != cudaSuccess) {
     cudaGetLastError();
     return TW_ERR_CUDA;
   }
-  *status = v ? v : g;
+  *status = v ? v : g ? g : m;
   return TW_OK;
 }
 
