@@ -139,8 +139,11 @@ TW_API tw_status tw_pack_ternary(const float *W, int64_t N, int64_t K, uint8_t *
  *   __device__ variable), which every GPU that loads the library holds until the
  *   process exits.  The call allocates nothing, frees nothing and calls no
  *   allocating routine; it clears the scratch on `stream` before use.
- *   The first call on a device looks up the scratch address (cudaGetSymbolAddress,
- *   with that device current); make that first call before any stream capture.
+ *   Every call looks up the scratch address afresh (cudaGetSymbolAddress, in the
+ *   current device's current context), so the call stays correct after
+ *   cudaDeviceReset or with another driver context made current; nothing from an
+ *   earlier call is reused.  The first call in a context loads the library's device
+ *   code there; make that first call before any stream capture.
  *   All calls share the one scratch array per device: calls whose work overlaps on
  *   the GPU (different streams, or other threads) race on it and may produce a wrong
  *   w_scale.  Serialise them, e.g. on one stream.

@@ -15,7 +15,6 @@
 //   workspace histogram with 64-bit global atomics; the last CTA to arrive
 //   (completion counter, no waiting) computes gamma.
 // Kernel 2 (pack): one thread per 32-bit output word (16 weights, 64 bytes of W).
-#include <atomic>
 
 #include "tw_common.cuh"
 
@@ -156,28 +155,19 @@ namespace {
 
 static __device__ __align__(256) tw::PackWorkspace g_pack_scratch;
 
-constexpr int kMaxScratchDevices = 64;
-std::atomic<uintptr_t> g_pack_scratch_addr[kMaxScratchDevices];  // device address, 0 = not set up
-
 }  // namespace
 
-// Device address of g_pack_scratch on the current device.  The first call on a
-// device looks it up with cudaGetSymbolAddress (in host code the symbol names a
-// host-side stand-in, never the device memory itself); later calls reuse it.
+// Device address of g_pack_scratch in the current device's current context (in
+// host code the symbol names a host-side stand-in, never the device memory
+// itself).  Looked up on every call rather than cached: after cudaDeviceReset, or
+// with another driver context made current, the module is loaded afresh and its
+// variables move, so an address kept from an earlier call could point into memory
+// that now belongs to someone else.
 cudaError_t tw_pack_scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_pack_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
-  uintptr_t v = g_pack_scratch_addr[dev].load(std::memory_order_acquire);
-  if (v == 0) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_pack_scratch);
-    if (e != cudaSuccess) return e;
-    v = reinterpret_cast<uintptr_t>(p);
-    g_pack_scratch_addr[dev].store(v, std::memory_order_release);
-  }
-  *out = reinterpret_cast<void*>(v);
+  *out = p;
   return cudaSuccess;
 }
 

@@ -62,7 +62,9 @@ def test_noalloc_after_a_different_tensor():
     tw, lib = _lib()
     Wa = si.device_normal((512, 1024), seed=11)
     Wb = 3.0 * si.device_normal((300, 640), seed=12)
-    _pack_noalloc_raw(lib, Wa)
+    st_a, packed_a, scale_a = _pack_noalloc_raw(lib, Wa)  # leaves Wa's histogram in the scratch
+    ref_packed_a, ref_scale_a = _pack_with_workspace(tw, Wa)
+    assert st_a == tw.TW_OK and scale_a == ref_scale_a and (packed_a == ref_packed_a).all()
     st, packed, scale = _pack_noalloc_raw(lib, Wb)
     ref_packed, ref_scale = _pack_with_workspace(tw, Wb)
     assert st == tw.TW_OK and scale == ref_scale and (packed == ref_packed).all()
