@@ -28,7 +28,7 @@ _lib_omp = None
 CFLAGS = ["-O2", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off",
           "-fno-fast-math", "-fno-unsafe-math-optimizations", "-frounding-math"]
 
-STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "invalid 2-bit code",
+STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "invalid code (2-bit field 3, byte > 242, or padding)",
           4: "non-finite input", 5: "negative value", 6: "int32 overflow"}
 
 
@@ -75,12 +75,18 @@ def _bind(lib):
         "two_rmsnorm": [p, p, ctypes.c_float, i64, i64, p, p],
         "two_rmsnorm_quant_act": [p, p, ctypes.c_float, i64, i64, p, p, p],
         "two_ternary_matmul": [p, ctypes.c_float, p, p, i64, i64, i64, p, p],
+        "two_pack_trits5": [p, i64, i64, p],
+        "two_unpack_trits5": [p, i64, i64, p],
+        "two_pack_ternary5": [p, i64, i64, p, p],
+        "two_ternary_matmul5": [p, ctypes.c_float, p, p, i64, i64, i64, p, p],
         "two_threads": [],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    lib.two_t5_row_bytes.argtypes = [i64]
+    lib.two_t5_row_bytes.restype = i64
     return lib
 
 
@@ -200,4 +206,54 @@ def ternary_matmul(packed, w_scale, x_q, s_x, openmp: bool = False):
     acc = np.zeros((M, N), np.int32)
     _check(_load(openmp).two_ternary_matmul(_ptr(packed), float(w_scale), _ptr(x_q), _ptr(s_x),
                                             M, N, K, _ptr(y), _ptr(acc)), "ternary_matmul")
+    return y, acc
+
+
+def t5_row_bytes(K: int) -> int:
+    """Bytes per row of the five-trits-per-byte layout: 16 * ceil(K / 80)."""
+    return int(_load().two_t5_row_bytes(int(K)))
+
+
+def pack_trits5(t):
+    """t int8 [N][K] in {-1, 0, 1} -> uint8 [N][t5_row_bytes(K)], five trits per byte."""
+    t = _c(t, np.int8)
+    N, K = t.shape
+    out = np.zeros((N, max(t5_row_bytes(K), 1)), np.uint8)
+    _check(_load().two_pack_trits5(_ptr(t), N, K, _ptr(out)), "pack_trits5")
+    return out
+
+
+def unpack_trits5(p5, K):
+    """Inverse of pack_trits5 -> t int8 [N][K]."""
+    p5 = _c(p5, np.uint8)
+    N = p5.shape[0]
+    t = np.zeros((N, K), np.int8)
+    _check(_load().two_unpack_trits5(_ptr(p5), N, K, _ptr(t)), "unpack_trits5")
+    return t
+
+
+def pack_ternary5(W):
+    """W fp32 [N][K] -> (uint8 [N][t5_row_bytes(K)], w_scale fp32): absmean ternarisation
+    stored five trits per byte."""
+    W = _c(W, np.float32)
+    N, K = W.shape
+    out = np.zeros((N, max(t5_row_bytes(K), 1)), np.uint8)
+    ws = np.zeros(1, np.float32)
+    _check(_load().two_pack_ternary5(_ptr(W), N, K, _ptr(out), _ptr(ws)), "pack_ternary5")
+    return out, np.float32(ws[0])
+
+
+def ternary_matmul5(p5, w_scale, x_q, s_x, openmp: bool = False):
+    """Rows stored five trits per byte, x_q int8 [M][K] -> (y fp32 [M][N], acc int32 [M][N])."""
+    p5 = _c(p5, np.uint8)
+    x_q = _c(x_q, np.int8)
+    if x_q.ndim == 1:
+        x_q = x_q[None, :]
+    s_x = _c(s_x, np.float32).ravel()
+    M, K = x_q.shape
+    N = p5.shape[0]
+    y = np.zeros((M, N), np.float32)
+    acc = np.zeros((M, N), np.int32)
+    _check(_load(openmp).two_ternary_matmul5(_ptr(p5), float(w_scale), _ptr(x_q), _ptr(s_x),
+                                             M, N, K, _ptr(y), _ptr(acc)), "ternary_matmul5")
     return y, acc

@@ -19,7 +19,8 @@
  *        an add) and section 3.2 (conversion absmean-quantises every weight
  *        onto the ternary set).
  *   [P5] "BitNet 1 位 LLM 独立推理引擎：位串行 GEMM 内核与 LUT 优化工程实践",
- *        正文 paragraph 4 (I2_S is the plain 2-bit format).
+ *        正文 paragraph 4 (I2_S is the plain 2-bit format) and paragraph 3 (TL2
+ *        packs several weights into one small index so fewer bytes are loaded).
  * The pages give no formula for absmean, the activation scale, the rounding
  * mode or the bit layout; this file follows these readings:
  *   - one absmean scale per tensor, gamma = mean |W| with the sum taken
@@ -33,6 +34,9 @@
  *   - RMSNorm: r = exact sum of x^2 rounded once to double,
  *     ms = (float)(r / K), inv = 1 / sqrtf(ms + eps) (fp32),
  *     u = fl(fl(x * inv) * g), then the activation quantisation above on u;
+ *   - five trits per byte (the denser layout): RB = 16 * ceil(K / 80) bytes
+ *     per row; byte i holds weights 4i..4i+3 as base-3 digits 0..3 and weight
+ *     4 RB + i as digit 4, each digit t + 1; weights at k >= K count as 0;
  *   - acc = sum_k t * x_q exactly (int64, must fit int32);
  *   - y = (float)(((double)acc * gamma * s_x) / 127.0).
  * Compile with -ffp-contract=off and without fast-math so every fp32 step is
@@ -226,6 +230,97 @@ int two_unpack_ternary(const uint8_t *packed, int64_t N, int64_t K, int8_t *t) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* Five trits per byte ([P5] 正文 paragraph 3: TL2 stores three weights in a  */
+/* 5-bit index so fewer bytes are loaded; 3^5 = 243 <= 256 takes the same    */
+/* idea to 1.6 bits per weight).  Reading of the layout (the page fixes none):*/
+/*   a row takes RB = 16 * ceil(K / 80) bytes;                                */
+/*   byte i of a row holds the weights k = 4i, 4i+1, 4i+2, 4i+3 as its base-3 */
+/*   digits 0..3 and the weight k = 4*RB + i as its digit 4:                  */
+/*     byte = sum_{j<4} (t[4i+j] + 1) * 3^j + (t[4*RB + i] + 1) * 81;         */
+/*   weights at k >= K count as t = 0.  Bytes 243..255 are invalid.           */
+/* ------------------------------------------------------------------------ */
+int64_t two_t5_row_bytes(int64_t K) { return K <= 0 ? 0 : 16 * ((K + 79) / 80); }
+
+/* Weight k of a row sits in byte `*byte` as base-3 digit `*digit`. */
+static void t5_place(int64_t k, int64_t RB, int64_t *byte, int *digit) {
+  if (k < 4 * RB) {
+    *byte = k / 4;
+    *digit = (int)(k % 4);
+  } else {
+    *byte = k - 4 * RB;
+    *digit = 4;
+  }
+}
+
+int two_pack_trits5(const int8_t *t, int64_t N, int64_t K, uint8_t *out) {
+  if (!t || !out) return TWO_ERR_NULL;
+  if (N <= 0 || K <= 0 || K % 4 != 0) return TWO_ERR_SHAPE;
+  const int64_t RB = two_t5_row_bytes(K);
+  for (int64_t n = 0; n < N; ++n) {
+    /* every digit starts as the code of t = 0 */
+    for (int64_t b = 0; b < RB; ++b) out[n * RB + b] = 1 + 3 + 9 + 27 + 81;
+    for (int64_t k = 0; k < K; ++k) {
+      int v = t[n * K + k];
+      if (v < -1 || v > 1) return TWO_ERR_INVALID_CODE;
+      int64_t b;
+      int d;
+      t5_place(k, RB, &b, &d);
+      int w = 1;
+      for (int j = 0; j < d; ++j) w *= 3;
+      out[n * RB + b] = (uint8_t)(out[n * RB + b] + v * w); /* code (v + 1) replaces code 1 */
+    }
+  }
+  return TWO_OK;
+}
+
+/* Inverse of two_pack_trits5.  A byte above 242, or a nonzero weight at k >= K,
+ * is an error. */
+int two_unpack_trits5(const uint8_t *p, int64_t N, int64_t K, int8_t *t) {
+  if (!p || !t) return TWO_ERR_NULL;
+  if (N <= 0 || K <= 0 || K % 4 != 0) return TWO_ERR_SHAPE;
+  const int64_t RB = two_t5_row_bytes(K);
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t b = 0; b < RB; ++b) {
+      int v = p[n * RB + b];
+      if (v > 242) return TWO_ERR_INVALID_CODE;
+      for (int d = 0; d < 5; ++d) {
+        int code = v % 3;
+        v /= 3;
+        int64_t k = d < 4 ? 4 * b + d : 4 * RB + b;
+        if (k < K) t[n * K + k] = (int8_t)(code - 1);
+        else if (code != 1) return TWO_ERR_INVALID_CODE;
+      }
+    }
+  }
+  return TWO_OK;
+}
+
+/* Absmean ternarisation (as two_pack_ternary) stored five trits per byte. */
+int two_pack_ternary5(const float *W, int64_t N, int64_t K, uint8_t *out, float *w_scale) {
+  if (!W || !out || !w_scale) return TWO_ERR_NULL;
+  if (N <= 0 || K <= 0 || K % 4 != 0) return TWO_ERR_SHAPE;
+  float gamma;
+  int st = two_absmean(W, N * K, &gamma, NULL);
+  if (st != TWO_OK) return st;
+  int8_t *t = (int8_t *)malloc((size_t)K);
+  if (!t) return TWO_ERR_NULL;
+  for (int64_t n = 0; n < N && st == TWO_OK; ++n) {
+    for (int64_t k = 0; k < K; ++k) {
+      float w = W[n * K + k];
+      if (!isfinite(w)) {
+        st = TWO_ERR_NONFINITE;
+        break;
+      }
+      t[k] = (int8_t)ternarise(w, gamma);
+    }
+    if (st == TWO_OK) st = two_pack_trits5(t, 1, K, out + n * two_t5_row_bytes(K));
+  }
+  free(t);
+  if (st == TWO_OK) *w_scale = gamma;
+  return st;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Per-token absmax int8 activation quantisation ([P2] 技术实现细节).        */
 /* ------------------------------------------------------------------------ */
 int two_quant_act(const float *x, int64_t M, int64_t K, int8_t *x_q, float *s_x,
@@ -340,6 +435,41 @@ int two_ternary_matmul(const uint8_t *packed, float w_scale, const int8_t *x_q,
     if (status != TWO_OK) return status;
   }
   return TWO_OK;
+}
+
+/* The product over rows stored five trits per byte: each row is decoded with
+ * two_unpack_trits5, then summed and dequantised exactly as two_ternary_matmul. */
+int two_ternary_matmul5(const uint8_t *p5, float w_scale, const int8_t *x_q, const float *s_x,
+                        int64_t M, int64_t N, int64_t K, float *y, int32_t *acc_out) {
+  if (!p5 || !x_q || !s_x || !y) return TWO_ERR_NULL;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 4 != 0) return TWO_ERR_SHAPE;
+  const int64_t RB = two_t5_row_bytes(K);
+  int status = TWO_OK;
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) {
+    int8_t *t = (int8_t *)malloc((size_t)K);
+    int bad = t ? two_unpack_trits5(p5 + n * RB, 1, K, t) : TWO_ERR_NULL;
+    for (int64_t m = 0; m < M && bad == TWO_OK; ++m) {
+      int64_t acc = 0;
+      for (int64_t k = 0; k < K; ++k) {
+        int xv = x_q[m * K + k];
+        if (t[k] == 1) acc += xv;
+        else if (t[k] == -1) acc -= xv;
+      }
+      if (acc > INT32_MAX || acc < INT32_MIN) {
+        bad = TWO_ERR_OVERFLOW;
+        break;
+      }
+      if (acc_out) acc_out[m * N + n] = (int32_t)acc;
+      y[m * N + n] = (float)(((double)acc * (double)w_scale * (double)s_x[m]) / 127.0);
+    }
+    free(t);
+    if (bad != TWO_OK) {
+#pragma omp atomic write
+      status = bad;
+    }
+  }
+  return status;
 }
 
 /* Threads the row loop above may use: 1 in the plain build. */
