@@ -28,8 +28,9 @@ roofline: the product kernel.  Average launch duration = the timed region's devi
 cpu_baseline / --impl reference: the CPU oracle (oracle/), as it stands, on the host.
 Default workload only, as extra keys: us_per_layer_unfused (the same step with the
 quantisations as separate kernels), small_case (K = N = 256, M = 1: microseconds per
-call, latency-bound) and read_stream (a read-only streaming rate, the third bandwidth
-basis next to the nominal 8 TB/s and the measured copy rate).
+call, latency-bound), read_stream (a read-only streaming rate, the third bandwidth
+basis next to the nominal 8 TB/s and the measured copy rate) and five_trits_per_byte
+(the 2B step and a 57344 x 8192 product in the 1.6-bit layout next to the 2-bit one).
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling,
 no data-path collective); rank 0 prints max-over-ranks time and the summed bytes.
@@ -110,6 +111,16 @@ def layer_plan(model=MODEL):
 def gemv_bytes(N, K, M=1):
     """Algorithmic bytes of one GEMV launch: packed weights + int8 activations + scales."""
     return N * K // 4 + M * K + 4 + 4 * M
+
+
+def t5_row_bytes(K):
+    """Bytes per row of the five-trits-per-byte layout: 16 ceil(K / 80)."""
+    return 16 * ((K + 79) // 80)
+
+
+def gemv_bytes_t5(N, K, M=1):
+    """Algorithmic bytes of one GEMV launch over five-trits-per-byte rows."""
+    return N * t5_row_bytes(K) + M * K + 4 + 4 * M
 
 
 def step_bytes(M=1, model=MODEL, layers=LAYERS):
@@ -355,10 +366,11 @@ class DecodeStack:
     `distinct` layers are drawn and packed from their own seeds; further layers are
     byte copies of them in their own memory (the stream is what is measured)."""
 
-    def __init__(self, tw, layers: int, M: int = 1, seed: int = 1234, model: str = MODEL, distinct=None):
+    def __init__(self, tw, layers: int, M: int = 1, seed: int = 1234, model: str = MODEL, distinct=None,
+                 layout: str = "2bit"):
         import torch
         import seeded_inputs as si
-        self.tw, self.M, self.layers, self.model = tw, M, layers, model
+        self.tw, self.M, self.layers, self.model, self.layout = tw, M, layers, model, layout
         self.plan = layer_plan(model)
         distinct = layers if distinct is None else distinct
         n_in = layers * sum(M * K for _, N, K, _ in self.plan)
@@ -374,11 +386,15 @@ class DecodeStack:
         for l in range(layers):
             d = {}
             for i, (name, N, K, pro) in enumerate(self.plan):
-                packed = torch.empty((N, K // 4), dtype=torch.uint8, device="cuda")
+                row_bytes = tw.tw_t5_row_bytes(K) if layout == "t5" else K // 4
+                packed = torch.empty((N, row_bytes), dtype=torch.uint8, device="cuda")
                 gamma = torch.empty(1, dtype=torch.float32, device="cuda")
                 if l < distinct:
                     W = si.device_normal((N, K), seed=seed + 1000 * l + i)
-                    tw.tw_pack_ternary(W, packed, gamma, ws)
+                    if layout == "t5":
+                        tw.tw_pack_ternary_t5(W, packed, gamma, ws)
+                    else:
+                        tw.tw_pack_ternary(W, packed, gamma, ws)
                     del W
                 else:
                     src = self.L[l % distinct][name]
@@ -412,6 +428,8 @@ class DecodeStack:
 
     def fused_ok(self, e):
         """Whether the fused quantisation + GEMV kernel takes this shape (decided once)."""
+        if self.layout == "t5":
+            return False
         key = (e["N"], e["K"])
         if key not in self._fused_ok:
             import seeded_inputs as si
@@ -445,7 +463,9 @@ class DecodeStack:
                 if events is not None:
                     a, b = events_new(), events_new()
                     a.record()
-                if fz:
+                if self.layout == "t5":
+                    tw.tw_ternary_gemv_t5(e["packed"], e["gamma"], e["x_q"], e["s_x"], e["y"])
+                elif fz:
                     tw.tw_quant_gemv(e["x"], e["packed"], e["gamma"], e["y"], g=e["g"], eps=si.RMS_EPS)
                 else:
                     tw.tw_ternary_matmul(e["packed"], e["gamma"], e["x_q"], e["s_x"], e["y"], e["x_sum"],
@@ -674,6 +694,70 @@ def per_shape_isolated(stack, fused, M, plan):
             for n, v in per_launch.items()}
 
 
+def t5_comparison(tw, steps: int, warmup: int, copies: int = 4, reps: int = 5):
+    """The five-trits-per-byte layout next to the 2-bit one: the 2B decode step (30 layers,
+    quantisation as its own kernel before each product, one CUDA graph) in both layouts,
+    and each layout's product alone on a large matrix (the 70B gate|up, 57344 x 8192, four
+    copies so the stream leaves L2).  Weights per second is the comparable figure: the
+    five-trit layout moves 20 % fewer bytes for the same weights."""
+    import torch
+    import seeded_inputs as si
+    out = {}
+    for layout in ("2bit", "t5"):
+        stack = DecodeStack(tw, LAYERS, M=1, layout=layout)
+        graph = capture(stack, fused=False)
+        for _ in range(warmup):
+            graph.replay()
+        el = timed_replays(graph, steps, 1)
+        plan = layer_plan(MODEL)
+        nbytes = LAYERS * sum((gemv_bytes_t5 if layout == "t5" else gemv_bytes)(N, K) for _, N, K, _ in plan)
+        weights = LAYERS * sum(N * K for _, N, K, _ in plan)
+        out[f"2b_step_{layout}"] = {"us_per_layer": el / steps / LAYERS * 1e6,
+                                    "GB/s": nbytes * steps / el / 1e9,
+                                    "Gweights/s": weights * steps / el / 1e9,
+                                    "bytes_per_step": nbytes, "launches_per_step": stack.launches_per_step(False)}
+        del graph, stack
+        torch.cuda.empty_cache()
+    N, K = 57344, 8192
+    ws = torch.empty(tw.tw_pack_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    x = si.device_normal((1, K), seed=5)
+    xq, sx, xs = tw.quantize(x)
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    for layout in ("2bit", "t5"):
+        packs = []
+        for c in range(copies):
+            W = si.device_normal((N, K), seed=300 + c)
+            packs.append(tw.pack_t5(W) if layout == "t5" else tw.pack(W))
+            del W
+
+        def one_pass():
+            for p, g in packs:
+                if layout == "t5":
+                    tw.tw_ternary_gemv_t5(p, g, xq, sx, y)
+                else:
+                    tw.tw_ternary_gemv(p, g, xq, sx, y, xs)
+
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            one_pass()
+        torch.cuda.current_stream().wait_stream(st)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_pass()
+        for _ in range(3):
+            graph.replay()
+        el = timed_replays(graph, reps, 1)
+        us = el / (reps * copies) * 1e6
+        nbytes = (gemv_bytes_t5 if layout == "t5" else gemv_bytes)(N, K)
+        out[f"gemv_{N}x{K}_{layout}"] = {"us_per_launch": us, "GB/s": nbytes / us / 1e3,
+                                          "Gweights/s": N * K / us / 1e3}
+        del graph, packs
+        torch.cuda.empty_cache()
+    return out
+
+
 # The other configurations, measured in the default run (each line's own roofline and CPU
 # baseline): small steps, since each workload's graph is replayed back to back.
 OTHER_WORKLOADS = ["2b_m8", "2b_m64", "2b_m256", "8b_m1", "8b_m16", "70b_m1", "70b_m4", "70b_m16"]
@@ -715,6 +799,7 @@ def run_ours(args):
     if default:
         extra["small_case"] = small_case_latency(tw)
         extra["read_stream"] = read_stream_rate()
+        extra["five_trits_per_byte"] = t5_comparison(tw, min(args.steps, 200), args.warmup)
     cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
     if default and cpu_ok:
         extra["small_case"]["cpu_oracle_us_per_call_single_thread"] = cpu_small_case_us()
@@ -782,7 +867,7 @@ def run_ours(args):
 def run_kernel_case(args):
     """Kernels in isolation (for timing sweeps and small ncu captures; not the contract line).
 
-    --kernel-case {gemv,fused,fused_rms,quant,rms_quant,gemm,gemm_nows,matmul} (a comma list) on --shape
+    --kernel-case {gemv,t5,fused,fused_rms,quant,rms_quant,gemm,gemm_nows,matmul} (a comma list) on --shape
     NxK at --M tokens (a comma list), over --copies distinct weight tensors (so the stream leaves
     L2); one pass over them is captured in a CUDA graph and replayed --reps times (device time
     per launch, host launch cost excluded).  One JSON line per (case, M)."""
@@ -792,24 +877,30 @@ def run_kernel_case(args):
     import ternary_weight_quant_b300 as tw
     N, K = (int(v) for v in args.shape.lower().split("x"))
     ws = torch.empty(tw.tw_pack_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
-    packs = []
+    cases = args.kernel_case.split(",")
+    packs, packs5 = [], []
     for c in range(args.copies):
         W = si.device_normal((N, K), seed=77 + c)
-        p = torch.empty((N, K // 4), dtype=torch.uint8, device="cuda")
-        g = torch.empty(1, dtype=torch.float32, device="cuda")
-        tw.tw_pack_ternary(W, p, g, ws)
+        if any(k != "t5" for k in cases):
+            p = torch.empty((N, K // 4), dtype=torch.uint8, device="cuda")
+            g = torch.empty(1, dtype=torch.float32, device="cuda")
+            tw.tw_pack_ternary(W, p, g, ws)
+            packs.append((p, g))
+        if "t5" in cases:
+            packs5.append(tw.pack_t5(W))
         del W
-        packs.append((p, g))
     gain = 1.0 + 0.1 * si.device_normal((K,), seed=6)
     for M in (int(v) for v in str(args.M).split(",")):
         x = si.device_normal((M, K), seed=5)
         xq, sx, xs = tw.quantize(x)
         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
         gws = tw.gemm_workspace(M, K)
-        for k in args.kernel_case.split(","):
+        for k in cases:
 
             def launch(p, g):
-                if k == "gemv":
+                if k == "t5":
+                    tw.tw_ternary_gemv_t5(p, g, xq, sx, y)
+                elif k == "gemv":
                     tw.tw_ternary_gemv(p, g, xq, sx, y, xs)
                 elif k in ("fused", "fused_rms"):
                     tw.tw_quant_gemv(x, p, g, y, g=gain if k == "fused_rms" else None)
@@ -827,7 +918,7 @@ def run_kernel_case(args):
                     raise SystemExit(f"unknown kernel case {k}")
 
             def one_pass():
-                for p, g in packs:
+                for p, g in (packs5 if k == "t5" else packs):
                     launch(p, g)
 
             try:
@@ -853,9 +944,11 @@ def run_kernel_case(args):
                 graph.replay()
             b.record()
             torch.cuda.synchronize()
-            us = a.elapsed_time(b) * 1e3 / (args.reps * len(packs))
+            us = a.elapsed_time(b) * 1e3 / (args.copies * args.reps)
+            nbytes = gemv_bytes_t5(N, K, M) if k == "t5" else gemv_bytes(N, K, M)
             print(json.dumps({"kernel_case": k, "N": N, "K": K, "M": M, "us_per_launch": us,
-                              "GB/s": gemv_bytes(N, K, M) / us / 1e3, "TFLOP/s": 2 * M * N * K / us / 1e6}),
+                              "GB/s": nbytes / us / 1e3, "Gweights/s": N * K / us / 1e3,
+                              "TFLOP/s": 2 * M * N * K / us / 1e6}),
                   flush=True)
             del graph
     return 0
@@ -879,7 +972,7 @@ def main():
                     help="default run: leave out the other configurations")
     ap.add_argument("--workload-steps", type=int, default=10, help="timed steps of each other configuration")
     ap.add_argument("--kernel-case", default=None,
-                    help="time one kernel alone: gemv, fused, fused_rms, quant, rms_quant, gemm, gemm_nows or matmul")
+                    help="time one kernel alone: gemv, t5, fused, fused_rms, quant, rms_quant, gemm, gemm_nows or matmul")
     ap.add_argument("--shape", default="13824x2560", help="NxK for --kernel-case")
     ap.add_argument("--M", default="1", help="tokens for --kernel-case (a comma list)")
     ap.add_argument("--copies", type=int, default=8, help="distinct weight tensors for --kernel-case")

@@ -271,6 +271,47 @@ TW_API tw_status tw_ternary_matmul(const uint8_t *packed, const float *w_scale, 
                                    size_t ws_bytes, tw_stream_t stream);
 
 /*
+ * The denser weight layout: five trits per byte, 1.6 bits per weight ("BitNet 1 位 LLM
+ * 独立推理引擎：位串行 GEMM 内核与 LUT 优化工程实践", 正文 paragraph 3: TL2 packs several
+ * ternary weights into one small table index so that fewer weight bytes are loaded; the
+ * "1bit-systems" page, 性能实测: the bandwidth-bound GEMV only gets faster by reading
+ * fewer bytes).  The pages fix no byte layout; this library's reading:
+ *   a row takes RB = 16 * ceil(K / 80) bytes (tw_t5_row_bytes(K); ceil(K / 5) rounded up
+ *   to whole 16-byte chunks, exactly K / 5 when K % 80 == 0); byte i of a row holds the
+ *   weights 4i, 4i+1, 4i+2, 4i+3 as base-3 digits 0..3 and the weight 4 RB + i as digit 4,
+ *   each digit t + 1 (byte = sum_j digit_j 3^j <= 242); weights at k >= K are 0.
+ * Returns 0 for K the calls below reject.
+ */
+TW_API size_t tw_t5_row_bytes(int64_t K);
+
+/*
+ * Absmean ternarisation (the same gamma and t as tw_pack_ternary) stored five trits per
+ * byte.
+ *   W          [N][K] fp32, 16-byte aligned.
+ *   packed5    [N][tw_t5_row_bytes(K)] uint8 output, 16-byte aligned.
+ *   w_scale, workspace, ws_bytes: as tw_pack_ternary (the same workspace size).
+ * Requires 1 <= N, 4 <= K <= TW_MAX_K, K % 4 == 0, N*K < TW_MAX_NK.
+ */
+TW_API tw_status tw_pack_ternary_t5(const float *W, int64_t N, int64_t K, uint8_t *packed5,
+                                    float *w_scale, void *workspace, size_t ws_bytes,
+                                    tw_stream_t stream);
+
+/*
+ * The ternary GEMV over rows stored five trits per byte: the same acc and y as
+ * tw_ternary_gemv on the same weights (exact int32 accumulators).  A 256-entry table in
+ * shared memory turns each byte into its five weights.
+ *   packed5  [N][tw_t5_row_bytes(K)] uint8 from tw_pack_ternary_t5, 16-byte aligned.
+ *   x_q      [M][K] int8, 16-byte aligned.   w_scale, s_x, y, acc_out: as tw_ternary_gemv.
+ * Requires 1 <= M <= 2, N >= 1, 16 <= K <= 40960, K % 16 == 0, N*K < TW_MAX_NK.  Bytes
+ * above 242 never come out of tw_pack_ternary_t5; the kernel reads them as zero weights.
+ * Launched with programmatic dependent launch: it builds its table before the previous
+ * kernel on `stream` has finished and reads x_q and s_x only after it has.
+ */
+TW_API tw_status tw_ternary_gemv_t5(const uint8_t *packed5, const float *w_scale, const int8_t *x_q,
+                                    const float *s_x, int64_t M, int64_t N, int64_t K, float *y,
+                                    int32_t *acc_out, tw_stream_t stream);
+
+/*
  * Reads and clears the library's device status word: 0, or TW_ERR_TIMEOUT when a
  * kernel gave up a bounded wait (it then left its outputs unwritten).  Synchronises
  * the current device; meant for diagnostics after a failed step, not the hot path.

@@ -50,6 +50,9 @@ def _load():
         "tw_gemm_workspace_bytes": ([i64, i64], sz),
         "tw_quant_gemv": ([p, p, ctypes.c_float, p, p, i64, i64, i64, p, p, p, p, p, p], ctypes.c_int),
         "tw_device_status": ([p], ctypes.c_int),
+        "tw_t5_row_bytes": ([i64], sz),
+        "tw_pack_ternary_t5": ([p, i64, i64, p, p, p, sz, p], ctypes.c_int),
+        "tw_ternary_gemv_t5": ([p, p, p, p, i64, i64, i64, p, p, p], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -170,6 +173,29 @@ def tw_quant_gemv(x, packed, w_scale, y, g=None, eps=1e-6, x_q=None, s_x=None, x
           _ptr(x_q), _ptr(s_x), _ptr(x_sum), _ptr(acc_out), _stream(stream))
 
 
+def tw_t5_row_bytes(K: int) -> int:
+    """Bytes per row of the five-trits-per-byte layout (0 for a K the calls reject)."""
+    return int(_lib.tw_t5_row_bytes(K))
+
+
+def tw_pack_ternary_t5(W, packed5, w_scale, workspace, N=None, K=None, stream=None):
+    """W fp32 [N][K] -> packed5 uint8 [N][tw_t5_row_bytes(K)] (five trits per byte), w_scale [1]."""
+    N = W.shape[0] if N is None else N
+    K = W.shape[1] if K is None else K
+    ws_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+    _call("tw_pack_ternary_t5", _ptr(W), N, K, _ptr(packed5), _ptr(w_scale), _ptr(workspace), ws_bytes,
+          _stream(stream))
+
+
+def tw_ternary_gemv_t5(packed5, w_scale, x_q, s_x, y, acc_out=None, M=None, N=None, K=None, stream=None):
+    """The GEMV over five-trits-per-byte rows (1 or 2 tokens)."""
+    M = x_q.shape[0] if M is None else M
+    K = x_q.shape[-1] if K is None else K
+    N = packed5.shape[0] if N is None else N
+    _call("tw_ternary_gemv_t5", _ptr(packed5), _ptr(w_scale), _ptr(x_q), _ptr(s_x), M, N, K, _ptr(y),
+          _ptr(acc_out), _stream(stream))
+
+
 def tw_device_status() -> int:
     """Read and clear the device status word (0 or a TW_ERR_* code); synchronises the device."""
     out = ctypes.c_int32(0)
@@ -186,6 +212,17 @@ def pack(W: torch.Tensor, stream=None):
     ws = torch.empty(max(tw_pack_workspace_bytes(N, K), 8), dtype=torch.uint8, device=W.device)
     tw_pack_ternary(W, packed, w_scale, ws, stream=stream)
     return packed, w_scale
+
+
+def pack_t5(W: torch.Tensor, stream=None):
+    """Allocate outputs and pack a device fp32 [N][K] tensor five trits per byte.
+    Returns (packed5, w_scale)."""
+    N, K = W.shape
+    packed5 = torch.empty((N, tw_t5_row_bytes(K)), dtype=torch.uint8, device=W.device)
+    w_scale = torch.empty(1, dtype=torch.float32, device=W.device)
+    ws = torch.empty(max(tw_pack_workspace_bytes(N, K), 8), dtype=torch.uint8, device=W.device)
+    tw_pack_ternary_t5(W, packed5, w_scale, ws, stream=stream)
+    return packed5, w_scale
 
 
 def quantize(x: torch.Tensor, g: torch.Tensor | None = None, eps: float = 1e-6, stream=None):

@@ -46,6 +46,11 @@ cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const in
                            int M, int N, int K, float* y, int32_t* acc_out, void* workspace, cudaStream_t stream,
                            int num_sms, int* unsupported);
 size_t tw_gemm_ws_size(long long M, long long K);
+cudaError_t tw_launch_pack_t5(const float* W, long long N, long long K, uint8_t* packed5, float* w_scale,
+                              void* workspace, cudaStream_t stream, int num_sms);
+int tw_t5_supported(int M, int N, int K);
+cudaError_t tw_launch_gemv_t5(const uint8_t* packed5, const float* w_scale, const int8_t* x_q, const float* s_x,
+                              int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream, int num_sms);
 
 namespace {
 
@@ -311,6 +316,42 @@ TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, 
   if (st != TW_OK) return st;
   return from_cuda(tw_launch_gemv_generic(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
                                           (cudaStream_t)stream));
+}
+
+TW_API size_t tw_t5_row_bytes(int64_t K) {
+  if (check_kdim(K) != TW_OK) return 0;
+  return (size_t)(16 * ((K + 79) / 80));
+}
+
+TW_API tw_status tw_pack_ternary_t5(const float* W, int64_t N, int64_t K, uint8_t* packed5, float* w_scale,
+                                    void* workspace, size_t ws_bytes, tw_stream_t stream) {
+  if (!W || !packed5 || !w_scale) return TW_ERR_NULL;
+  if (N < 1 || check_kdim(K) != TW_OK || N * K >= TW_MAX_NK) return TW_ERR_SHAPE;
+  if (!workspace || ws_bytes < tw_pack_ws_size()) return TW_ERR_WORKSPACE;
+  if (!aligned(W, 16) || !aligned(packed5, 16) || !aligned(w_scale, 4) || !aligned(workspace, 8))
+    return TW_ERR_ALIGN;
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(W, packed5, w_scale, static_cast<const uint8_t*>(workspace));
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_pack_t5(W, N, K, packed5, w_scale, workspace, (cudaStream_t)stream, sms));
+}
+
+TW_API tw_status tw_ternary_gemv_t5(const uint8_t* packed5, const float* w_scale, const int8_t* x_q,
+                                    const float* s_x, int64_t M, int64_t N, int64_t K, float* y,
+                                    int32_t* acc_out, tw_stream_t stream) {
+  tw_status st = check_product_args(packed5, w_scale, x_q, s_x, M, N, K, y);
+  if (st != TW_OK) return st;
+  if (M > 2 || !tw_t5_supported((int)M, (int)N, (int)K)) return TW_ERR_SHAPE;
+  if (!aligned(packed5, 16) || !aligned(x_q, 16) || !aligned(acc_out, 4)) return TW_ERR_ALIGN;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != TW_OK) return st;
+  st = check_device_ptrs(packed5, w_scale, x_q, s_x, y, acc_out);
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_gemv_t5(packed5, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
+                                     (cudaStream_t)stream, sms));
 }
 
 TW_API tw_status tw_device_status(int32_t* status) {

@@ -108,11 +108,45 @@ __global__ void __launch_bounds__(256) pack_kernel(const float4* __restrict__ W4
   }
 }
 
+// Five trits per byte (the 1.6-bit layout).  A row takes RB = 16 ceil(K / 80) bytes; byte
+// i holds the weights 4i..4i+3 as base-3 digits 0..3 and the weight 4 RB + i as digit 4,
+// each digit t + 1 (t = 0 past K).  One thread per 4-byte word of the output (20 weights):
+// the 16 weights of digits 0..3 are four float4 loads, the 4 of digit 4 one more.
+__global__ void __launch_bounds__(256) pack_t5_kernel(const float* __restrict__ W, long long N, int K, int RB,
+                                                      const float* __restrict__ w_scale,
+                                                      uint32_t* __restrict__ out) {
+  const float gamma = *w_scale;
+  const int wpr = RB / 4;
+  const long long total = N * wpr;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);  // t = 0 for any gamma
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long n = i / wpr;
+    const int q = (int)(i - n * wpr);
+    const float* row = W + n * (long long)K;
+    const int kf = 4 * RB + 4 * q;
+    const float4 f = kf < K ? __ldcs(reinterpret_cast<const float4*>(row + kf)) : zero;
+    const float fifth[4] = {f.x, f.y, f.z, f.w};
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int kq = 16 * q + 4 * b;
+      const float4 v = kq < K ? __ldcs(reinterpret_cast<const float4*>(row + kq)) : zero;
+      const uint32_t byte = ternary_code(v.x, gamma) + 3u * ternary_code(v.y, gamma) +
+                            9u * ternary_code(v.z, gamma) + 27u * ternary_code(v.w, gamma) +
+                            81u * ternary_code(fifth[b], gamma);
+      word |= byte << (8 * b);
+    }
+    out[i] = word;
+  }
+}
+
 }  // namespace tw
 
 // Host launcher (called from tw_api.cu after argument checks).
-cudaError_t tw_launch_pack(const float* W, long long N, long long K, uint8_t* packed, float* w_scale,
-                           void* workspace, cudaStream_t stream, int num_sms) {
+// absmean: clears the workspace, then the histogram kernel writes gamma to w_scale.
+static cudaError_t launch_absmean(const float* W, long long N, long long K, float* w_scale, void* workspace,
+                                  cudaStream_t stream, int num_sms) {
   using namespace tw;
   PackWorkspace* ws = static_cast<PackWorkspace*>(workspace);
   cudaError_t err = cudaMemsetAsync(ws, 0, sizeof(PackWorkspace), stream);
@@ -127,9 +161,15 @@ cudaError_t tw_launch_pack(const float* W, long long N, long long K, uint8_t* pa
   if (blocks < 1) blocks = 1;
   absmean_hist_kernel<<<(unsigned)blocks, 512, 0, stream>>>(reinterpret_cast<const float4*>(W), n4, ws,
                                                             w_scale, n);
-  err = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+cudaError_t tw_launch_pack(const float* W, long long N, long long K, uint8_t* packed, float* w_scale,
+                           void* workspace, cudaStream_t stream, int num_sms) {
+  using namespace tw;
+  cudaError_t err = launch_absmean(W, N, K, w_scale, workspace, stream, num_sms);
   if (err != cudaSuccess) return err;
-  const long long nbytes = n / 4;
+  const long long nbytes = N * K / 4;
   long long pblocks = (nbytes / 4 + 255) / 256;
   const long long pmax = (long long)num_sms * 8;
   if (pblocks > pmax) pblocks = pmax;
@@ -140,6 +180,23 @@ cudaError_t tw_launch_pack(const float* W, long long N, long long K, uint8_t* pa
 }
 
 size_t tw_pack_ws_size() { return sizeof(tw::PackWorkspace); }
+
+// The same absmean, then the five-trits-per-byte layout (RB = 16 ceil(K / 80) bytes per row).
+cudaError_t tw_launch_pack_t5(const float* W, long long N, long long K, uint8_t* packed5, float* w_scale,
+                              void* workspace, cudaStream_t stream, int num_sms) {
+  using namespace tw;
+  cudaError_t err = launch_absmean(W, N, K, w_scale, workspace, stream, num_sms);
+  if (err != cudaSuccess) return err;
+  const int RB = (int)(16 * ((K + 79) / 80));
+  const long long words = N * (RB / 4);
+  long long blocks = (words + 255) / 256;
+  const long long bmax = (long long)num_sms * 8;
+  if (blocks > bmax) blocks = bmax;
+  if (blocks < 1) blocks = 1;
+  pack_t5_kernel<<<(unsigned)blocks, 256, 0, stream>>>(W, N, (int)K, RB, w_scale,
+                                                       reinterpret_cast<uint32_t*>(packed5));
+  return cudaGetLastError();
+}
 
 // ----------------------------------------------------------------------------
 // Allocation-free variant: the same two kernels with their scratch in a

@@ -154,3 +154,22 @@ def test_import_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import ternary_weight_quant_b300"], cwd=str(tmp_path),
                        capture_output=True, text=True, env={**os.environ, "PYTHONPATH": str(tmp_path)})
     assert r.returncode != 0 and "libtw.so not built" in r.stderr
+
+
+def test_t5_row_bytes_and_checks(tw):
+    lib = tw.lib()
+    assert [tw.tw_t5_row_bytes(K) for K in (4, 80, 84, 2560, 6912)] == [16, 16, 32, 512, 1392]
+    assert tw.tw_t5_row_bytes(0) == 0 and tw.tw_t5_row_bytes(6) == 0 and tw.tw_t5_row_bytes(65536) == 0
+    # pack: NULL, shape, workspace, alignment (packed5 must be 16-byte aligned)
+    assert lib.tw_pack_ternary_t5(None, 4, 16, FAKE, FAKE, FAKE, 4096, None) == tw.TW_ERR_NULL
+    assert lib.tw_pack_ternary_t5(FAKE, 4, 6, FAKE, FAKE, FAKE, 4096, None) == tw.TW_ERR_SHAPE
+    assert lib.tw_pack_ternary_t5(FAKE, 4, 16, FAKE, FAKE, FAKE, 8, None) == tw.TW_ERR_WORKSPACE
+    assert lib.tw_pack_ternary_t5(FAKE, 4, 16, FAKE + 4, FAKE, FAKE, 4096, None) == tw.TW_ERR_ALIGN
+    # GEMV: 1 or 2 tokens, K % 16 == 0, K <= 40960, 16-byte aligned packed5 and x_q
+    g = lambda M, K, p5=FAKE, xq=FAKE: lib.tw_ternary_gemv_t5(p5, FAKE, xq, FAKE, M, 8, K, FAKE, None, None)
+    assert lib.tw_ternary_gemv_t5(FAKE, FAKE, None, FAKE, 1, 8, 64, FAKE, None, None) == tw.TW_ERR_NULL
+    assert g(3, 64) == tw.TW_ERR_SHAPE
+    assert g(1, 68) == tw.TW_ERR_SHAPE
+    assert g(1, 40976) == tw.TW_ERR_SHAPE
+    assert g(1, 64, p5=FAKE + 4) == tw.TW_ERR_ALIGN
+    assert g(2, 64, xq=FAKE + 8) == tw.TW_ERR_ALIGN
