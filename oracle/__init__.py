@@ -75,6 +75,8 @@ def _bind(lib):
         "two_rmsnorm": [p, p, ctypes.c_float, i64, i64, p, p],
         "two_rmsnorm_quant_act": [p, p, ctypes.c_float, i64, i64, p, p, p],
         "two_ternary_matmul": [p, ctypes.c_float, p, p, i64, i64, i64, p, p],
+        "two_rms_inv": [p, ctypes.c_float, i64, i64, p],
+        "two_residual_add": [p, p, i64, p],
         "two_pack_trits5": [p, i64, i64, p],
         "two_unpack_trits5": [p, i64, i64, p],
         "two_pack_ternary5": [p, i64, i64, p, p],
@@ -176,6 +178,27 @@ def rmsnorm(x, g, eps):
     r = np.zeros(M, np.float64)
     _check(_load().two_rmsnorm(_ptr(x), _ptr(g), float(eps), M, K, _ptr(u), _ptr(r)), "rmsnorm")
     return u, r
+
+
+def rms_inv(x, eps):
+    """Per row 1 / sqrtf(ms + eps), the RMSNorm scale (fp32 [M])."""
+    x = _c(x, np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    M, K = x.shape
+    inv = np.zeros(M, np.float32)
+    _check(_load().two_rms_inv(_ptr(x), float(eps), M, K, _ptr(inv)), "rms_inv")
+    return inv
+
+
+def residual_add(h, y):
+    """fl32(h + y) element by element."""
+    h = _c(h, np.float32)
+    y = _c(y, np.float32)
+    assert h.shape == y.shape
+    out = np.zeros(h.shape, np.float32)
+    _check(_load().two_residual_add(_ptr(h), _ptr(y), h.size, _ptr(out)), "residual_add")
+    return out
 
 
 def rmsnorm_quant_act(x, g, eps):

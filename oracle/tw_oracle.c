@@ -37,6 +37,7 @@
  *   - five trits per byte (the denser layout): RB = 16 * ceil(K / 80) bytes
  *     per row; byte i holds weights 4i..4i+3 as base-3 digits 0..3 and weight
  *     4 RB + i as digit 4, each digit t + 1; weights at k >= K count as 0;
+ *   - residual: h_out = fl32(h + y);
  *   - acc = sum_k t * x_q exactly (int64, must fit int32);
  *   - y = (float)(((double)acc * gamma * s_x) / 127.0).
  * Compile with -ffp-contract=off and without fast-math so every fp32 step is
@@ -358,23 +359,46 @@ int two_quant_act(const float *x, int64_t M, int64_t K, int8_t *x_q, float *s_x,
 /* ------------------------------------------------------------------------ */
 /* RMSNorm ([P1] 技术架构; constants are this file's reading).               */
 /* ------------------------------------------------------------------------ */
+/* 1 / sqrtf(ms + eps) of one row, ms = (float)(r / K), r = the exact sum of squares
+ * rounded once to double (returned in *r_out). */
+static int rms_inv_row(const float *row, int64_t K, float eps, float *inv_out, double *r_out) {
+  big_t acc;
+  big_clear(&acc);
+  for (int64_t k = 0; k < K; ++k) {
+    if (!isfinite(row[k])) return TWO_ERR_NONFINITE;
+    double v = (double)row[k];
+    big_add_double(&acc, v * v); /* the square of a float is exact in double */
+  }
+  double r = big_to_double(&acc);
+  *r_out = r;
+  float ms = (float)(r / (double)K);
+  *inv_out = 1.0f / sqrtf(ms + eps);
+  return TWO_OK;
+}
+
+/* The RMSNorm scale alone, per row. */
+int two_rms_inv(const float *x, float eps, int64_t M, int64_t K, float *inv) {
+  if (!x || !inv) return TWO_ERR_NULL;
+  if (M <= 0 || K <= 0) return TWO_ERR_SHAPE;
+  for (int64_t m = 0; m < M; ++m) {
+    double r;
+    int st = rms_inv_row(x + m * K, K, eps, inv + m, &r);
+    if (st != TWO_OK) return st;
+  }
+  return TWO_OK;
+}
+
 int two_rmsnorm(const float *x, const float *g, float eps, int64_t M, int64_t K,
                 float *u, double *sumsq_out) {
   if (!x || !g || !u) return TWO_ERR_NULL;
   if (M <= 0 || K <= 0) return TWO_ERR_SHAPE;
   for (int64_t m = 0; m < M; ++m) {
     const float *row = x + m * K;
-    big_t acc;
-    big_clear(&acc);
-    for (int64_t k = 0; k < K; ++k) {
-      if (!isfinite(row[k])) return TWO_ERR_NONFINITE;
-      double v = (double)row[k];
-      big_add_double(&acc, v * v); /* the square of a float is exact in double */
-    }
-    double r = big_to_double(&acc);
+    double r;
+    float inv;
+    int st = rms_inv_row(row, K, eps, &inv, &r);
+    if (st != TWO_OK) return st;
     if (sumsq_out) sumsq_out[m] = r;
-    float ms = (float)(r / (double)K);
-    float inv = 1.0f / sqrtf(ms + eps);
     for (int64_t k = 0; k < K; ++k) {
       float t = row[k] * inv;
       u[m * K + k] = t * g[k];
@@ -393,6 +417,21 @@ int two_rmsnorm_quant_act(const float *x, const float *g, float eps, int64_t M,
   if (st == TWO_OK) st = two_quant_act(u, M, K, x_q, s_x, x_sum);
   free(u);
   return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Residual add after an output projection ("1-bit 大模型官方推理框架", summary */
+/* on kernel fusion: the add is fused into the product's epilogue on the GPU): */
+/* h_out = fl32(h + y), one IEEE fp32 addition per element.                   */
+/* ------------------------------------------------------------------------ */
+int two_residual_add(const float *h, const float *y, int64_t n, float *out) {
+  if (!h || !y || !out) return TWO_ERR_NULL;
+  if (n <= 0) return TWO_ERR_SHAPE;
+  for (int64_t i = 0; i < n; ++i) {
+    if (!isfinite(h[i]) || !isfinite(y[i])) return TWO_ERR_NONFINITE;
+    out[i] = h[i] + y[i];
+  }
+  return TWO_OK;
 }
 
 /* ------------------------------------------------------------------------ */
