@@ -30,7 +30,9 @@ Default workload only, as extra keys: us_per_layer_unfused (the same step with t
 quantisations as separate kernels), small_case (K = N = 256, M = 1: microseconds per
 call, latency-bound), read_stream (a read-only streaming rate, the third bandwidth
 basis next to the nominal 8 TB/s and the measured copy rate) and five_trits_per_byte
-(the 2B step and a 57344 x 8192 product in the 1.6-bit layout next to the 2-bit one).
+(the 2B step and a 57344 x 8192 product in the 1.6-bit layout next to the 2-bit one) and
+fused_epilogue (the 2B step with the residual add and the next RMSNorm's statistics fused
+into the o and down launches).
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling,
 no data-path collective); rank 0 prints max-over-ranks time and the summed bytes.
@@ -694,6 +696,86 @@ def per_shape_isolated(stack, fused, M, plan):
             for n, v in per_launch.items()}
 
 
+def epilogue_chain(tw, steps: int, warmup: int):
+    """The 2B decode step (30 layers, one token) with the fused epilogues: q|k|v and gate|up
+    quantise from the partial statistics the o and down launches left, which add their
+    output to the residual stream in their epilogue.  Per layer: q|k|v (RMSNorm from finished
+    statistics), o (quantisation of its synthetic input, GEMV, residual add, statistics of
+    the next RMSNorm), gate|up (as q|k|v), down (as o).  One residual buffer, updated in
+    place; one CUDA graph per step, timed like the main line."""
+    import torch
+    import seeded_inputs as si
+    stack = DecodeStack(tw, LAYERS, M=1)
+    hid = layer_plan(MODEL)[1][1]  # o: N = hidden
+    h = si.device_normal((hid,), seed=77)
+    ws = tw.epilogue_workspace()
+    gains = [1.0 + 0.1 * si.device_normal((hid,), seed=900 + i) for i in range(2 * LAYERS)]
+
+    def enqueue():
+        for l, d in enumerate(stack.L):
+            g_attn, g_ffn = gains[2 * l], gains[2 * l + 1]
+            g_attn_next = gains[(2 * l + 2) % (2 * LAYERS)]
+            e = d["qkv"]
+            tw.tw_quant_gemv_stats(h, g_attn, ws, e["packed"], e["gamma"], e["y"], eps=si.RMS_EPS)
+            e = d["o"]
+            tw.tw_quant_gemv_residual(e["x"], e["packed"], e["gamma"], h, h, g_ffn, ws, eps=si.RMS_EPS, y=e["y"])
+            e = d["gateup"]
+            tw.tw_quant_gemv_stats(h, g_ffn, ws, e["packed"], e["gamma"], e["y"], eps=si.RMS_EPS)
+            e = d["down"]
+            tw.tw_quant_gemv_residual(e["x"], e["packed"], e["gamma"], h, h, g_attn_next, ws, eps=si.RMS_EPS,
+                                      y=e["y"])
+
+    def enqueue_unfused():
+        # the same dataflow without the epilogue: RMSNorm over h in the q|k|v and gate|up
+        # launches, the residual adds as separate (library) kernels after o and down
+        h2 = h.view(1, -1)
+        for l, d in enumerate(stack.L):
+            g_attn, g_ffn = gains[2 * l], gains[2 * l + 1]
+            e = d["qkv"]
+            tw.tw_quant_gemv(h2, e["packed"], e["gamma"], e["y"], g=g_attn, eps=si.RMS_EPS)
+            e = d["o"]
+            tw.tw_quant_gemv(e["x"], e["packed"], e["gamma"], e["y"])
+            h2.add_(e["y"])
+            e = d["gateup"]
+            tw.tw_quant_gemv(h2, e["packed"], e["gamma"], e["y"], g=g_ffn, eps=si.RMS_EPS)
+            e = d["down"]
+            tw.tw_quant_gemv(e["x"], e["packed"], e["gamma"], e["y"])
+            h2.add_(e["y"])
+
+    def timed(fn):
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            fn()
+        torch.cuda.current_stream().wait_stream(st)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        for _ in range(warmup):
+            graph.replay()
+        el = timed_replays(graph, steps, 1)
+        del graph
+        return el
+
+    # statistics for the very first q|k|v: one down-projection residual call
+    e = stack.L[-1]["down"]
+    tw.tw_quant_gemv_residual(e["x"], e["packed"], e["gamma"], h, h, gains[0], ws, y=e["y"])
+    el = timed(enqueue)
+    status = tw.tw_device_status()
+    el_unfused = timed(enqueue_unfused)
+    nbytes = step_bytes(1)
+    del stack
+    torch.cuda.empty_cache()
+    return {"us_per_layer": el / steps / LAYERS * 1e6, "GB/s": nbytes * steps / el / 1e9,
+            "bytes_per_step": nbytes, "launches_per_step": 4 * LAYERS, "device_status": status,
+            "chain": "qkv (RMSNorm from finished statistics) -> o (+ residual, next statistics) -> gate|up "
+                     "(finished statistics) -> down (+ residual, next statistics)",
+            "us_per_layer_residual_unfused": el_unfused / steps / LAYERS * 1e6,
+            "unfused": "the same dataflow: RMSNorm + quantisation fused into each GEMV launch, the two residual "
+                       "adds as separate torch kernels (6 launches per layer)"}
+
+
 def t5_comparison(tw, steps: int, warmup: int, copies: int = 4, reps: int = 5):
     """The five-trits-per-byte layout next to the 2-bit one: the 2B decode step (30 layers,
     quantisation as its own kernel before each product, one CUDA graph) in both layouts,
@@ -800,6 +882,7 @@ def run_ours(args):
         extra["small_case"] = small_case_latency(tw)
         extra["read_stream"] = read_stream_rate()
         extra["five_trits_per_byte"] = t5_comparison(tw, min(args.steps, 200), args.warmup)
+        extra["fused_epilogue"] = epilogue_chain(tw, args.steps, args.warmup)
     cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
     if default and cpu_ok:
         extra["small_case"]["cpu_oracle_us_per_call_single_thread"] = cpu_small_case_us()

@@ -271,6 +271,58 @@ TW_API tw_status tw_ternary_matmul(const uint8_t *packed, const float *w_scale, 
                                    size_t ws_bytes, tw_stream_t stream);
 
 /*
+ * Fused epilogues for one decode token ("1-bit 大模型官方推理框架：低显存低功耗 LLM 部署方案",
+ * its summary on kernel fusion and FAQ 2 on how the dequantised values are used): the
+ * residual add after a layer's output projections, and the partial statistics of the
+ * following RMSNorm, formed where the GEMV writes its outputs, so that the next quantisation
+ * starts from them instead of reducing over its input first.
+ *
+ * Workspace (bytes) that carries those statistics from tw_quant_gemv_residual to
+ * tw_quant_gemv_stats: one 16-byte partial per CTA of the writing launch.  Its contents on
+ * entry to tw_quant_gemv_residual do not matter.
+ */
+TW_API size_t tw_epilogue_workspace_bytes(void);
+
+/*
+ * tw_quant_gemv for one token (M = 1; RMSNorm when g != NULL) with the residual epilogue:
+ *   y       = acc * gamma * s_x / 127 as the definitions state it (in double, one rounding
+ *             to fp32: bit-identical to that expression), written when y != NULL;
+ *   h_out   = fl32(h + y) for each of the N outputs (h_out may be h);
+ *   workspace: the partial statistics of h_out for the RMSNorm with gain g_next that reads
+ *             it next (tw_quant_gemv_stats): per CTA a float-float sum of squares of its
+ *             outputs and the output with the largest fl(|h_out g_next|).
+ *   x, g, eps, packed, w_scale, acc_out: as tw_quant_gemv.   h, h_out: [N] fp32, 16-byte
+ *   aligned.   g_next: [N] fp32.   workspace: tw_epilogue_workspace_bytes() bytes, 16-byte
+ *   aligned.
+ * Requires 64 <= N <= 8192 and N % 64 == 0, 64 <= K <= 8192 and K % 64 == 0;
+ * TW_ERR_UNSUPPORTED when the one-token kernel's shared memory does not hold the CTA's
+ * share of the weights.  Launched with programmatic dependent launch as tw_quant_gemv (g_next
+ * is also read before the previous kernel has finished).
+ */
+TW_API tw_status tw_quant_gemv_residual(const float *x, const float *g, float eps, const uint8_t *packed,
+                                        const float *w_scale, int64_t N, int64_t K, const float *h,
+                                        float *h_out, const float *g_next, float *y, int32_t *acc_out,
+                                        void *workspace, size_t ws_bytes, tw_stream_t stream);
+
+/*
+ * tw_quant_gemv for one token with RMSNorm, its statistics taken from the workspace that the
+ * tw_quant_gemv_residual which wrote x left: every CTA folds the partials (float-float sum
+ * of squares; 1 / rms decided exactly as the RMSNorm definition states, from x itself when
+ * the sum cannot decide the rounding) and takes the candidate scale from the output with the
+ * largest fl(|x g|); the quantisation checks every |u| against it and takes the true largest
+ * |u| when one exceeds it.  The results equal tw_quant_gemv(x, g, eps, ...) exactly.
+ *   x: [K] fp32 (the h_out of that call), 16-byte aligned.   g: [K] gain (its g_next).
+ *   workspace: as that call left it (for x with K = its N), 16-byte aligned.
+ *   Other arguments as tw_quant_gemv.
+ * Requires N >= 1, 64 <= K <= 8192, K % 64 == 0; TW_ERR_UNSUPPORTED as above.  The workspace
+ * is read after the previous kernel on `stream` has finished (programmatic dependent launch).
+ */
+TW_API tw_status tw_quant_gemv_stats(const float *x, const float *g, float eps, const void *workspace,
+                                     const uint8_t *packed, const float *w_scale, int64_t N, int64_t K,
+                                     float *y, int8_t *x_q_out, float *s_x_out, int32_t *x_sum_out,
+                                     int32_t *acc_out, tw_stream_t stream);
+
+/*
  * The denser weight layout: five trits per byte, 1.6 bits per weight ("BitNet 1 位 LLM
  * 独立推理引擎：位串行 GEMM 内核与 LUT 优化工程实践", 正文 paragraph 3: TL2 packs several
  * ternary weights into one small table index so that fewer weight bytes are loaded; the

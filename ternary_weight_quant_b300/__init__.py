@@ -50,6 +50,9 @@ def _load():
         "tw_gemm_workspace_bytes": ([i64, i64], sz),
         "tw_quant_gemv": ([p, p, ctypes.c_float, p, p, i64, i64, i64, p, p, p, p, p, p], ctypes.c_int),
         "tw_device_status": ([p], ctypes.c_int),
+        "tw_epilogue_workspace_bytes": ([], sz),
+        "tw_quant_gemv_residual": ([p, p, ctypes.c_float, p, p, i64, i64, p, p, p, p, p, p, sz, p], ctypes.c_int),
+        "tw_quant_gemv_stats": ([p, p, ctypes.c_float, p, p, p, i64, i64, p, p, p, p, p, p], ctypes.c_int),
         "tw_t5_row_bytes": ([i64], sz),
         "tw_pack_ternary_t5": ([p, i64, i64, p, p, p, sz, p], ctypes.c_int),
         "tw_ternary_gemv_t5": ([p, p, p, p, i64, i64, i64, p, p, p], ctypes.c_int),
@@ -171,6 +174,36 @@ def tw_quant_gemv(x, packed, w_scale, y, g=None, eps=1e-6, x_q=None, s_x=None, x
     N = packed.shape[0] if N is None else N
     _call("tw_quant_gemv", _ptr(x), _ptr(g), float(eps), _ptr(packed), _ptr(w_scale), M, N, K, _ptr(y),
           _ptr(x_q), _ptr(s_x), _ptr(x_sum), _ptr(acc_out), _stream(stream))
+
+
+def tw_epilogue_workspace_bytes() -> int:
+    return int(_lib.tw_epilogue_workspace_bytes())
+
+
+def epilogue_workspace(device="cuda"):
+    """Allocate the workspace that carries the statistics from tw_quant_gemv_residual to
+    tw_quant_gemv_stats."""
+    return torch.empty(tw_epilogue_workspace_bytes(), dtype=torch.uint8, device=device)
+
+
+def tw_quant_gemv_residual(x, packed, w_scale, h, h_out, g_next, workspace, g=None, eps=1e-6, y=None,
+                           acc_out=None, N=None, K=None, stream=None):
+    """One token: (RMSNorm +) quantisation + GEMV, then h_out = h + y and the partial
+    statistics of the next RMSNorm (gain g_next) into workspace."""
+    K = x.shape[-1] if K is None else K
+    N = packed.shape[0] if N is None else N
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _call("tw_quant_gemv_residual", _ptr(x), _ptr(g), float(eps), _ptr(packed), _ptr(w_scale), N, K, _ptr(h),
+          _ptr(h_out), _ptr(g_next), _ptr(y), _ptr(acc_out), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def tw_quant_gemv_stats(x, g, workspace, packed, w_scale, y, eps=1e-6, x_q=None, s_x=None, x_sum=None,
+                        acc_out=None, N=None, K=None, stream=None):
+    """One token: RMSNorm from the statistics a residual epilogue left + quantisation + GEMV."""
+    K = x.shape[-1] if K is None else K
+    N = packed.shape[0] if N is None else N
+    _call("tw_quant_gemv_stats", _ptr(x), _ptr(g), float(eps), _ptr(workspace), _ptr(packed), _ptr(w_scale), N, K,
+          _ptr(y), _ptr(x_q), _ptr(s_x), _ptr(x_sum), _ptr(acc_out), _stream(stream))
 
 
 def tw_t5_row_bytes(K: int) -> int:

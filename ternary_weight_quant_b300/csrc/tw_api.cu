@@ -46,6 +46,17 @@ cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const in
                            int M, int N, int K, float* y, int32_t* acc_out, void* workspace, cudaStream_t stream,
                            int num_sms, int* unsupported);
 size_t tw_gemm_ws_size(long long M, long long K);
+size_t tw_epi_ws_size();
+int tw_decode_residual_supported(int N, int K, int num_sms, int rms);
+int tw_decode_stats_supported(int N, int K, int num_sms);
+cudaError_t tw_launch_quant_gemv_residual(const float* x, const float* g, float eps, const uint8_t* packed,
+                                          const float* w_scale, int N, int K, const float* res, float* res_out,
+                                          const float* g_next, float* y, int32_t* acc_out, void* parts,
+                                          cudaStream_t stream, int num_sms, bool pdl);
+cudaError_t tw_launch_quant_gemv_stats(const float* x, const float* g, float eps, const void* parts,
+                                       const uint8_t* packed, const float* w_scale, int N, int K, float* y,
+                                       int8_t* x_q_out, float* s_x_out, int32_t* x_sum_out, int32_t* acc_out,
+                                       cudaStream_t stream, int num_sms, bool pdl);
 cudaError_t tw_launch_pack_t5(const float* W, long long N, long long K, uint8_t* packed5, float* w_scale,
                               void* workspace, cudaStream_t stream, int num_sms);
 int tw_t5_supported(int M, int N, int K);
@@ -352,6 +363,51 @@ TW_API tw_status tw_ternary_gemv_t5(const uint8_t* packed5, const float* w_scale
   if (st != TW_OK) return st;
   return from_cuda(tw_launch_gemv_t5(packed5, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
                                      (cudaStream_t)stream, sms));
+}
+
+TW_API size_t tw_epilogue_workspace_bytes(void) { return tw_epi_ws_size(); }
+
+TW_API tw_status tw_quant_gemv_residual(const float* x, const float* g, float eps, const uint8_t* packed,
+                                        const float* w_scale, int64_t N, int64_t K, const float* h, float* h_out,
+                                        const float* g_next, float* y, int32_t* acc_out, void* workspace,
+                                        size_t ws_bytes, tw_stream_t stream) {
+  if (!x || !packed || !w_scale || !h || !h_out || !g_next) return TW_ERR_NULL;
+  if (N < 64 || N > 8192 || N % 64 != 0 || check_kdim(K) != TW_OK || K % 64 != 0 || K > 8192) return TW_ERR_SHAPE;
+  if (!workspace || ws_bytes < tw_epi_ws_size()) return TW_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(packed, 16) || !aligned(w_scale, 4) || !aligned(h, 16) ||
+      !aligned(h_out, 16) || !aligned(g_next, 4) || !aligned(y, 4) || !aligned(acc_out, 4) ||
+      !aligned(workspace, 16))
+    return TW_ERR_ALIGN;
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  if (!tw_decode_residual_supported((int)N, (int)K, sms, g != nullptr)) return TW_ERR_UNSUPPORTED;
+  st = check_device_ptrs(x, g, packed, w_scale, h, h_out, g_next, y, acc_out, static_cast<const uint8_t*>(workspace));
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_quant_gemv_residual(x, g, eps, packed, w_scale, (int)N, (int)K, h, h_out, g_next, y,
+                                                 acc_out, workspace, (cudaStream_t)stream, sms, true));
+}
+
+TW_API tw_status tw_quant_gemv_stats(const float* x, const float* g, float eps, const void* workspace,
+                                     const uint8_t* packed, const float* w_scale, int64_t N, int64_t K, float* y,
+                                     int8_t* x_q_out, float* s_x_out, int32_t* x_sum_out, int32_t* acc_out,
+                                     tw_stream_t stream) {
+  if (!x || !g || !workspace || !packed || !w_scale || !y) return TW_ERR_NULL;
+  if (N < 1 || N > (1LL << 31) - 1 || check_kdim(K) != TW_OK || K % 64 != 0 || K > 8192 || N * K >= TW_MAX_NK)
+    return TW_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(workspace, 16) || !aligned(packed, 16) ||
+      !aligned(w_scale, 4) || !aligned(y, 4) || !aligned(x_q_out, 16) || !aligned(s_x_out, 4) ||
+      !aligned(x_sum_out, 4) || !aligned(acc_out, 4))
+    return TW_ERR_ALIGN;
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  if (!tw_decode_stats_supported((int)N, (int)K, sms)) return TW_ERR_UNSUPPORTED;
+  st = check_device_ptrs(x, g, static_cast<const uint8_t*>(workspace), packed, w_scale, y, x_q_out, s_x_out,
+                         x_sum_out, acc_out);
+  if (st != TW_OK) return st;
+  return from_cuda(tw_launch_quant_gemv_stats(x, g, eps, workspace, packed, w_scale, (int)N, (int)K, y, x_q_out,
+                                              s_x_out, x_sum_out, acc_out, (cudaStream_t)stream, sms, true));
 }
 
 TW_API tw_status tw_device_status(int32_t* status) {

@@ -69,7 +69,24 @@ struct StreamArgs {
   int8_t* x_q_out;        // fused: written by CTA 0 when non-NULL
   float* s_x_out;
   int32_t* x_sum_out;
+  // one token, residual epilogue: res_out = fl(res + y) (y as the definition states, in
+  // double); each CTA stores the partial statistics of its rows of res_out for the next
+  // RMSNorm (gain g_next) as parts[CTA] = {float-float sum of squares (hi, lo), and the
+  // element h with its gain g of the largest fl(|h g|)}
+  const float* res;
+  float* res_out;
+  const float* g_next;
+  KDiv kd127;             // division by 127 (the exact y)
+  float4* parts_out;
+  int h_off;              // byte offset of the CTA's res_out values and g_next values in shared memory
+  // one token, finished statistics: the nparts partials a residual epilogue left for x
+  const float4* parts_in;
+  int nparts;
 };
+
+// Partials of the residual epilogue: one float4 per CTA of the writing launch (its grid is
+// min(N, SMs) <= kDecThreads).
+constexpr int kMaxEpiParts = 512;
 
 // Block-wide sum of MT values (every thread gets the results).
 template <int MT>
@@ -641,7 +658,6 @@ struct DecodeRed {
   float4 cg[kDecWarps];   // ... and of the gain
   uint32_t am[kDecWarps]; // re-check: per-warp largest |u|
   int qs[kDecWarps];      // per-warp sums of x_q
-  int viol;               // some |u_k| exceeded the candidate scale
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -674,11 +690,12 @@ __device__ __forceinline__ bool dec_mbar_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ int dec_unit(int q) { return q * kDecThreads + (int)threadIdx.x; }
 
 // Quantises this thread's float4s of x (registers xv, and the gain gv when RMS) with scale
-// amax into xs.  Returns the thread's sum of x_q; sets *viol when `check` and some |u| > amax.
+// amax into xs (and x_q_out when wout).  Returns the thread's sum of x_q; sets viol when
+// `check` and some |u| > amax.
 template <bool RMS, int NV>
 __device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, const float4 (&xv)[NV],
                                                const float4 (&gv)[NV], float inv, float amax, float ra,
-                                               bool check, int* viol) {
+                                               bool check, bool& viol, bool wout) {
   const int K4 = a.K >> 2;
   unsigned char* xsb = reinterpret_cast<unsigned char*>(xs);
   // d = fl(fl(u 127) ra) is within 2^-22 |d| < 3.1e-5 of fl(u 127) / a (|d| <= 127 once
@@ -736,7 +753,7 @@ __device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, c
     const int u = dec_unit(q);
     if (u < K4) {
       qsum = __dp4a((int)pq[q], 0x01010101, qsum);
-      if (blockIdx.x == 0 && a.x_q_out) reinterpret_cast<uint32_t*>(a.x_q_out)[u] = pq[q];
+      if (wout && a.x_q_out) reinterpret_cast<uint32_t*>(a.x_q_out)[u] = pq[q];
       // element k of 16-element group k/16 goes to byte (k/4) % 4 of word k % 4
       unsigned char* gb = xsb + (u >> 2) * 16 + (u & 3);
       gb[0] = (unsigned char)pq[q];
@@ -745,7 +762,7 @@ __device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, c
       gb[12] = (unsigned char)(pq[q] >> 24);
     }
   }
-  if (bad) *viol = 1;
+  viol = bad;
   return qsum;
 }
 
@@ -753,7 +770,9 @@ __device__ __forceinline__ int decode_quantise(const StreamArgs& a, uint4* xs, c
 // a = max |u|; sets *cs to the dequantisation scale fl(fl(gamma a) / 127) and *xtot to the
 // sum of x_q over the whole row.  A thread's float4s are units dec_unit(q), q < NV
 // (NV * kDecThreads >= K / 4); gv holds the gain's (RMS: loaded before the dependency wait).
-template <bool RMS, int NV>
+// STATS (RMS only): the sum of squares and the scale candidate come from the partials a
+// residual epilogue left (a.parts_in): no first pass over x and no block reduction.
+template <bool RMS, int NV, bool STATS = false>
 __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs, float4 (&gv)[NV], DecodeRed& r,
                                                  uint32_t* red_u, unsigned long long* red_lo,
                                                  unsigned long long* red_hi, uint32_t (*limb)[256],
@@ -763,15 +782,29 @@ __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs,
   const unsigned full = 0xffffffffu;
   const int K = a.K, K4 = K >> 2;
   const float4* xg = reinterpret_cast<const float4*>(a.x);
+  static_assert(!STATS || RMS, "finished statistics are those of an RMSNorm");
   float4 xv[NV];
 #pragma unroll
   for (int q = 0; q < NV; ++q) xv[q] = dec_unit(q) < K4 ? __ldcg(xg + dec_unit(q)) : make_float4(0.f, 0.f, 0.f, 0.f);
 
-  // ---- pass 1 (padding float4s are zero: they add nothing)
+  float amax, inv = 1.0f;
+  {
+  // ---- pass 1 (padding float4s are zero: they add nothing).  STATS: thread t takes the
+  // residual epilogue's partial t instead (a float-float sum of squares and the element
+  // with the largest fl(|h g|)), and everything below is the same.
   FF s0 = {0.0f, 0.0f}, s1 = {0.0f, 0.0f}, s2 = {0.0f, 0.0f}, s3 = {0.0f, 0.0f};
   float pmf = 0.0f;
   float4 cxv = make_float4(0.f, 0.f, 0.f, 0.f), cgv = cxv;
-  {
+  if constexpr (STATS) {
+    if (tid < a.nparts) {
+      const float4 pp = __ldcg(a.parts_in + tid);
+      s0.hi = pp.x;
+      s0.lo = pp.y;
+      pmf = fabsf(__fmul_rn(pp.z, pp.w));
+      cxv.x = pp.z;
+      cgv.x = pp.w;
+    }
+  } else {
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
       const float4 v = xv[q];
@@ -813,13 +846,11 @@ __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs,
     if (lane == 0) r.ff[warp] = make_float2(s0.hi, s0.lo);
   }
   if (lane == 0) r.pm[warp] = wm;
-  if (tid == 0) r.viol = 0;
   __syncthreads();  // (1) per-warp results
 
   // ---- every warp: combine (kDecWarps <= 16 partials, one per lane)
   const uint32_t ml = lane < kDecWarps ? r.pm[lane] : 0u;
   const uint32_t bm = __reduce_max_sync(full, ml);
-  float amax, inv = 1.0f;
   if constexpr (!RMS) {
     amax = __uint_as_float(bm);
   } else {
@@ -850,6 +881,7 @@ __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs,
     amax = fmaxf(fmaxf(fabsf(__fmul_rn(__fmul_rn(v.x, inv), gg.x)), fabsf(__fmul_rn(__fmul_rn(v.y, inv), gg.y))),
                  fmaxf(fabsf(__fmul_rn(__fmul_rn(v.z, inv), gg.z)), fabsf(__fmul_rn(__fmul_rn(v.w, inv), gg.w))));
   }
+  }
   *cs = dequant_scale(gam, amax);
 
   // ---- quantisation.  With RMSNorm the first pass checks the candidate scale; when some
@@ -858,11 +890,12 @@ __device__ __forceinline__ float decode_prologue(const StreamArgs& a, uint4* xs,
   for (int pass = 0;; ++pass) {
     float ra = amax == 0.0f ? 0.0f : __int_as_float(0x7fffffff);
     if (amax >= 0x1p-120f && amax <= 0x1p120f) asm("rcp.approx.f32 %0, %1;" : "=f"(ra) : "f"(amax));
-    int qs = decode_quantise<RMS, NV>(a, xs, xv, gv, inv, amax, ra, RMS && pass == 0, &r.viol);
+    bool bad = false;
+    int qs = decode_quantise<RMS, NV>(a, xs, xv, gv, inv, amax, ra, RMS && pass == 0, bad, blockIdx.x == 0);
     qs = __reduce_add_sync(full, qs);
     if (lane == 0) r.qs[warp] = qs;
-    __syncthreads();  // (2) xs and the per-warp sums complete; r.viol final
-    if (!RMS || pass > 0 || !r.viol) break;
+    const bool viol = __syncthreads_or(bad);  // (2) xs and the per-warp sums complete
+    if (!RMS || pass > 0 || !viol) break;
     float m = 0.0f;
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
@@ -911,10 +944,62 @@ __device__ __forceinline__ void decode_rows(const uint32_t* wsm, int Kw, int G, 
     tot[q] = __reduce_add_sync(0xffffffffu, acc[q][0] + (acc[q][1] >> 2) + (acc[q][2] >> 4) + (acc[q][3] >> 6));
 }
 
+// y = acc gamma s_x / 127 as the definition states it: ((acc gamma) s_x) / 127 in double,
+// then rounded to fp32 (the residual epilogue adds exactly this value).  The two products
+// are double multiplies (the first is exact); the division by 127 and both roundings are
+// done with integers (div_k_round_f32, d127 = make_kdiv(127)), so no double-precision
+// divide runs on this part's narrow double pipe.  |p| lies in [2^-298, 2^280]: a normal double.
+__device__ __forceinline__ float dequant_exact(int acc, float gamma, float s_x, const KDiv& d127) {
+  const double p = __dmul_rn(__dmul_rn((double)acc, (double)gamma), (double)s_x);
+  const unsigned long long b = (unsigned long long)__double_as_longlong(p);
+  if (p == 0.0) return (b >> 63) ? -0.0f : 0.0f;  // the signed zero of the double expression
+  const int be = (int)((b >> 52) & 0x7ffull);
+  const float q = div_k_round_f32((b & ((1ull << 52) - 1)) | (1ull << 52), be - 1075, d127);
+  return (b >> 63) ? -q : q;
+}
+
+// Residual epilogue, after the CTA's rows of res_out are written (hb: their values, gb: the
+// next gain at those rows): warp 0 stores the CTA's partial statistics (float-float sum of
+// squares, and the element with the largest fl(|h g|)).  Nothing waits: the launch that reads
+// the partials does so after griddepcontrol.wait, when this whole grid has finished.
+__device__ __forceinline__ void decode_epilogue(const StreamArgs& a, int nrows, const float* hb, const float* gb) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
+  FF t = {0.0f, 0.0f};
+  float pmf = 0.0f, hc = 0.0f, gc = 0.0f;
+  for (int rr = lane; rr < nrows; rr += 32) {
+    const float h = hb[rr], gg = gb[rr];
+    ff_add_square(t, h);
+    const float pv = fabsf(__fmul_rn(h, gg));
+    if (pv > pmf) {
+      pmf = pv;
+      hc = h;
+      gc = gg;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FF u;
+    u.hi = __shfl_xor_sync(full, t.hi, o);
+    u.lo = __shfl_xor_sync(full, t.lo, o);
+    ff_add(t, u);
+  }
+  const uint32_t pm = __float_as_uint(pmf);
+  const uint32_t wm = __reduce_max_sync(full, pm);
+  const int sel = __ffs(__ballot_sync(full, pm == wm)) - 1;
+  hc = __shfl_sync(full, hc, sel);
+  gc = __shfl_sync(full, gc, sel);
+  if (lane == 0) a.parts_out[blockIdx.x] = make_float4(t.hi, t.lo, hc, gc);
+}
+
 // The fused one-token GEMV (see above).  Dynamic shared memory: the CTA's packed rows at
 // offset 0 (plus slack for the last row's reads past its slice), xs (a.xs_off), the row
-// totals (a.acc_off, used when S > 1).
-template <int JMAX, int NV, bool RMS>
+// totals (a.acc_off, used when S > 1), and with the residual epilogue the CTA's res_out and
+// g_next values (a.h_off).
+// MODE 0: as above.  MODE 1: residual epilogue (y exact as defined; res_out = fl(res + y);
+// partial statistics for the next RMSNorm).  MODE 2: RMSNorm from the partial statistics a
+// residual epilogue left for x (no first pass over x, no block reduction before quantising).
+template <int JMAX, int NV, bool RMS, int MODE = 0>
 __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -927,13 +1012,15 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
   int* sacc = reinterpret_cast<int*>(smem + a.acc_off);          // [nrows] (S > 1)
   __shared__ DecodeRed red;
   __shared__ __align__(8) unsigned long long wbar;
-  __shared__ uint32_t red_u[RMS ? kDecWarps : 1];
-  __shared__ unsigned long long red_lo[RMS ? kDecWarps : 1], red_hi[RMS ? kDecWarps : 1];
+  constexpr bool kExact = RMS;  // the exact RMSNorm fallback may run
+  __shared__ uint32_t red_u[kExact ? kDecWarps : 1];
+  __shared__ unsigned long long red_lo[kExact ? kDecWarps : 1], red_hi[kExact ? kDecWarps : 1];
   __shared__ float s_inv[1];
   __shared__ int s_slow[1];
   __shared__ double s_dbl;
-  __shared__ uint32_t limb[RMS ? 3 : 1][256];
-  __shared__ unsigned long long hist[RMS ? 256 : 1];
+  __shared__ uint32_t limb[kExact ? 3 : 1][256];
+  __shared__ unsigned long long hist[kExact ? 256 : 1];
+  float* hb = reinterpret_cast<float*>(smem + a.h_off);  // MODE 1: [nrows] res_out values, then [nrows] g_next
 
   pdl_launch_dependents();
 
@@ -957,6 +1044,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
   const int S = a.S, G = kDecWarps / S;
   if (S > 1)
     for (int i = tid; i < nrows; i += kDecThreads) sacc[i] = 0;
+  if constexpr (MODE == 1) {  // the next gain at this CTA's rows is a parameter too
+    for (int i = tid; i < nrows; i += kDecThreads) {
+      hb[i] = 0.0f;
+      hb[nrows + i] = __ldg(a.g_next + row0 + i);
+    }
+  }
+  if (MODE == 1 && S == 1)
+    for (int i = tid; i < nrows; i += kDecThreads) sacc[i] = 0;
   float4 gv[NV];  // this thread's float4s of the RMSNorm gain
 #pragma unroll
   for (int q = 0; q < NV; ++q) {
@@ -972,11 +1067,27 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
   for (int i = tid; i < (K >> 5); i += kDecThreads)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(a.x + (size_t)i * 32) : "memory");
   pdl_wait();
+  float resv = 0.0f;  // MODE 1: the residual at this thread's row (rows one per thread), in flight with x
+  if (MODE == 1 && tid < nrows) resv = __ldcg(a.res + row0 + tid);
 
   float cs;
   int xtot;
-  const float amax = decode_prologue<RMS, NV>(a, xs, gv, red, red_u, red_lo, red_hi, limb, hist, &s_dbl, s_inv,
-                                              s_slow, gam, &cs, &xtot);
+  const float amax = decode_prologue<RMS, NV, MODE == 2>(a, xs, gv, red, red_u, red_lo, red_hi, limb, hist, &s_dbl,
+                                                          s_inv, s_slow, gam, &cs, &xtot);
+  // one row's outputs (MODE 1: y as defined, then the residual; rv = res at that row)
+  auto store_row = [&](int rr, int acc, float rv) {
+    const int n = row0 + rr;
+    if constexpr (MODE == 1) {
+      const float yv = dequant_exact(acc, gam, amax, a.kd127);
+      const float hv = __fadd_rn(rv, yv);
+      a.res_out[n] = hv;
+      hb[rr] = hv;
+      if (a.y) a.y[n] = yv;
+    } else {
+      a.y[n] = dequant(acc, cs, gam, amax);
+    }
+    if (a.acc_out) a.acc_out[n] = acc;
+  };
   const bool cs_normal = cs >= 1.17549435e-38f;
 
   uint4 xr[JMAX];
@@ -997,7 +1108,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
         for (int q = 0; q < 4; ++q) {
           if (q < n) {
             const int rr = gr + (i0 + q) * G;  // row within the CTA
-            if (S == 1) {
+            if (MODE == 1 && S == 1) {
+              sacc[rr] = tot[q];  // outputs below, one row per thread
+            } else if (S == 1) {
               const int acc = tot[q] - xtot;
               a.y[row0 + rr] = cs_normal ? __fmul_rn((float)acc, cs) : dequant_tiny(acc, gam, amax);
               if (a.acc_out) a.acc_out[row0 + rr] = acc;
@@ -1022,14 +1135,16 @@ __global__ void __launch_bounds__(kDecThreads, 2) gemv_decode_kernel(StreamArgs 
       emit(i0, 1, tot);
     }
   }
-  if (S > 1) {  // block-uniform
+  if (S > 1 || MODE == 1) {  // block-uniform
     if (!__syncthreads_or(!arrived)) {
-      for (int rr = tid; rr < nrows; rr += kDecThreads) {
-        const int acc = sacc[rr] - xtot;
-        a.y[row0 + rr] = dequant(acc, cs, gam, amax);
-        if (a.acc_out) a.acc_out[row0 + rr] = acc;
-      }
+      if (MODE == 1 && tid < nrows) store_row(tid, sacc[tid] - xtot, resv);  // nrows <= kDecThreads
+      for (int rr = tid + (MODE == 1 ? kDecThreads : 0); rr < nrows; rr += kDecThreads)
+        store_row(rr, sacc[rr] - xtot, MODE == 1 ? __ldcg(a.res + row0 + rr) : 0.0f);
     }
+  }
+  if constexpr (MODE == 1) {
+    __syncthreads();  // hb complete
+    if (warp == 0) decode_epilogue(a, nrows, hb, hb + nrows);
   }
   // a warp that gave up must not let the CTA exit while the copy may still land in shared
   // memory: one more bounded wait
@@ -1043,6 +1158,7 @@ namespace {
 struct Plan {
   int grid, rows_base, rows_rem, S, jmax;
   int xs_off, acc_off, xf_off;
+  int h_off = 0;
   size_t smem;
 };
 
@@ -1121,7 +1237,7 @@ cudaError_t launch(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, 
 // next launch); the CTA's packed rows, x_q and the row totals in dynamic shared memory, at
 // most kDecodeSmemMax bytes, and x in at most 4 (with RMSNorm) or 8 float4s per thread.  False otherwise
 // (the caller then takes gemv_stream_kernel).
-bool make_decode_plan(int N, int K, int num_sms, bool rms, Plan& p) {
+bool make_decode_plan(int N, int K, int num_sms, bool rms, Plan& p, bool epi = false) {
   if (K % 64 != 0 || K / 4 > (rms ? 4 : 8) * tw::kDecThreads) return false;
   const int Kw = K / 16;
   p.S = 0;
@@ -1144,13 +1260,17 @@ bool make_decode_plan(int N, int K, int num_sms, bool rms, Plan& p) {
   p.xs_off = (int)up(max_rows * (size_t)(K / 4) + slack, 128);
   p.acc_off = p.xs_off + (int)up((size_t)K, 16);
   p.xf_off = -1;
-  p.smem = (size_t)p.acc_off + (p.S > 1 ? up(max_rows * 4, 16) : 0);
+  p.smem = (size_t)p.acc_off + (p.S > 1 || epi ? up(max_rows * 4, 16) : 0);
+  if (epi) {  // the CTA's res_out values and g_next values
+    p.h_off = (int)up(p.smem, 16);
+    p.smem = (size_t)p.h_off + up(2 * max_rows * 4, 16);
+  }
   return p.smem <= kDecodeSmemMax;
 }
 
-template <int JMAX, int NV, bool RMS>
+template <int JMAX, int NV, bool RMS, int MODE = 0>
 cudaError_t launch_decode(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, bool pdl) {
-  auto kern = tw::gemv_decode_kernel<JMAX, NV, RMS>;
+  auto kern = tw::gemv_decode_kernel<JMAX, NV, RMS, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
   // every kernel of a decode chain asks for the same (largest) shared-memory carveout, so
@@ -1173,30 +1293,32 @@ cudaError_t launch_decode(const tw::StreamArgs& a, const Plan& p, cudaStream_t s
 // The kernel's template arguments follow from the plan: JMAX = words per lane and row, NV =
 // float4s of x per thread, ceil(K / 4 / kDecThreads) rounded up to 2, 4 or 8 (2 when one warp
 // spans K, S = 1; up to 4 with two K slices; 8, without RMSNorm only, with four).
-template <bool RMS>
+// MODE 1 and 2 (residual epilogue, finished statistics) take x in at most 4 float4s per
+// thread (K <= 8192).
+template <bool RMS, int MODE = 0>
 cudaError_t dispatch_decode(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, bool pdl) {
   const int nv = (a.K / 4 + tw::kDecThreads - 1) / tw::kDecThreads;
   if (nv <= 2) {
     switch (p.jmax) {
-      case 1: return launch_decode<1, 2, RMS>(a, p, stream, pdl);
-      case 2: return launch_decode<2, 2, RMS>(a, p, stream, pdl);
-      case 3: return launch_decode<3, 2, RMS>(a, p, stream, pdl);
-      case 4: return launch_decode<4, 2, RMS>(a, p, stream, pdl);
-      case 5: return launch_decode<5, 2, RMS>(a, p, stream, pdl);
-      case 6: return launch_decode<6, 2, RMS>(a, p, stream, pdl);
-      case 7: return launch_decode<7, 2, RMS>(a, p, stream, pdl);
-      case 8: return launch_decode<8, 2, RMS>(a, p, stream, pdl);
+      case 1: return launch_decode<1, 2, RMS, MODE>(a, p, stream, pdl);
+      case 2: return launch_decode<2, 2, RMS, MODE>(a, p, stream, pdl);
+      case 3: return launch_decode<3, 2, RMS, MODE>(a, p, stream, pdl);
+      case 4: return launch_decode<4, 2, RMS, MODE>(a, p, stream, pdl);
+      case 5: return launch_decode<5, 2, RMS, MODE>(a, p, stream, pdl);
+      case 6: return launch_decode<6, 2, RMS, MODE>(a, p, stream, pdl);
+      case 7: return launch_decode<7, 2, RMS, MODE>(a, p, stream, pdl);
+      case 8: return launch_decode<8, 2, RMS, MODE>(a, p, stream, pdl);
       default: break;
     }
   } else if (nv <= 4) {
     switch (p.jmax) {
-      case 5: return launch_decode<5, 4, RMS>(a, p, stream, pdl);
-      case 6: return launch_decode<6, 4, RMS>(a, p, stream, pdl);
-      case 7: return launch_decode<7, 4, RMS>(a, p, stream, pdl);
-      case 8: return launch_decode<8, 4, RMS>(a, p, stream, pdl);
+      case 5: return launch_decode<5, 4, RMS, MODE>(a, p, stream, pdl);
+      case 6: return launch_decode<6, 4, RMS, MODE>(a, p, stream, pdl);
+      case 7: return launch_decode<7, 4, RMS, MODE>(a, p, stream, pdl);
+      case 8: return launch_decode<8, 4, RMS, MODE>(a, p, stream, pdl);
       default: break;
     }
-  } else if constexpr (!RMS) {
+  } else if constexpr (!RMS && MODE == 0) {
     switch (p.jmax) {
       case 5: return launch_decode<5, 8, RMS>(a, p, stream, pdl);
       case 6: return launch_decode<6, 8, RMS>(a, p, stream, pdl);
@@ -1231,7 +1353,15 @@ cudaError_t dispatch(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream
 
 void fill_plan(tw::StreamArgs& a, const Plan& p) {
   a.rows_base = p.rows_base; a.rows_rem = p.rows_rem; a.S = p.S; a.xs_off = p.xs_off; a.acc_off = p.acc_off;
-  a.xf_off = p.xf_off;
+  a.xf_off = p.xf_off; a.h_off = p.h_off;
+}
+
+// The one-token decode kernel with the residual epilogue or with finished statistics takes
+// (N, K) when its plan fits (epilogue: with the per-row buffers) and x needs at most 4
+// float4s per thread.
+bool decode_mode_plan(int N, int K, int num_sms, bool rms, bool epi, Plan& p) {
+  if (K / 4 > 4 * tw::kDecThreads) return false;
+  return make_decode_plan(N, K, num_sms, rms, p, epi);
 }
 
 }  // namespace
@@ -1274,6 +1404,58 @@ cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, cons
   }
   if (g) return dispatch<true, true>(a, p, stream, pdl);
   return dispatch<true, false>(a, p, stream, pdl);
+}
+
+size_t tw_epi_ws_size() { return sizeof(float4) * tw::kMaxEpiParts; }
+
+// Partials a residual epilogue over N outputs leaves: one per CTA of its grid.
+int tw_epi_parts(int N, int num_sms) { return N < num_sms ? N : num_sms; }
+
+// 1 when the residual-epilogue decode (rms: with RMSNorm on x) takes (N, K), N = the next
+// RMSNorm's length, and the finished-statistics decode takes (N2 = any, K = N).
+int tw_decode_residual_supported(int N, int K, int num_sms, int rms) {
+  Plan p;
+  if (N % 64 != 0 || N / 4 > 4 * tw::kDecThreads || num_sms > tw::kMaxEpiParts) return 0;
+  return decode_mode_plan(N, K, num_sms, rms != 0, true, p) ? 1 : 0;
+}
+
+int tw_decode_stats_supported(int N, int K, int num_sms) {
+  Plan p;
+  if (num_sms > tw::kMaxEpiParts) return 0;
+  return decode_mode_plan(N, K, num_sms, true, false, p) ? 1 : 0;
+}
+
+cudaError_t tw_launch_quant_gemv_residual(const float* x, const float* g, float eps, const uint8_t* packed,
+                                          const float* w_scale, int N, int K, const float* res, float* res_out,
+                                          const float* g_next, float* y, int32_t* acc_out, void* parts,
+                                          cudaStream_t stream, int num_sms, bool pdl) {
+  Plan p;
+  if (!decode_mode_plan(N, K, num_sms, g != nullptr, true, p)) return cudaErrorInvalidValue;
+  tw::StreamArgs a = {};
+  a.packed = packed; a.w_scale = w_scale; a.x = x; a.g = g; a.eps = eps; a.kd = tw::make_kdiv(K);
+  a.inv_k = 1.0f / (float)K;
+  a.M = 1; a.N = N; a.K = K; a.y = y; a.acc_out = acc_out;
+  a.res = res; a.res_out = res_out; a.g_next = g_next; a.parts_out = static_cast<float4*>(parts);
+  a.kd127 = tw::make_kdiv(127);
+  fill_plan(a, p);
+  return g ? dispatch_decode<true, 1>(a, p, stream, pdl) : dispatch_decode<false, 1>(a, p, stream, pdl);
+}
+
+cudaError_t tw_launch_quant_gemv_stats(const float* x, const float* g, float eps, const void* parts,
+                                       const uint8_t* packed, const float* w_scale, int N, int K, float* y,
+                                       int8_t* x_q_out, float* s_x_out, int32_t* x_sum_out, int32_t* acc_out,
+                                       cudaStream_t stream, int num_sms, bool pdl) {
+  Plan p;
+  if (!decode_mode_plan(N, K, num_sms, true, false, p)) return cudaErrorInvalidValue;
+  tw::StreamArgs a = {};
+  a.packed = packed; a.w_scale = w_scale; a.x = x; a.g = g; a.eps = eps; a.kd = tw::make_kdiv(K);
+  a.inv_k = 1.0f / (float)K;
+  a.M = 1; a.N = N; a.K = K; a.y = y; a.acc_out = acc_out;
+  a.x_q_out = x_q_out; a.s_x_out = s_x_out; a.x_sum_out = x_sum_out;
+  a.parts_in = static_cast<const float4*>(parts);
+  a.nparts = tw_epi_parts(K, num_sms);
+  fill_plan(a, p);
+  return dispatch_decode<true, 2>(a, p, stream, pdl);
 }
 
 // Reads and clears the device status word (synchronous; diagnostics only).
