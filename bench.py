@@ -70,7 +70,7 @@ WORKLOADS = {
 SHAPE_TEXT = {"2B": "hidden 2560, ffn 6912, 20/5 heads", "8B": "hidden 4096, ffn 14336, 32/8 heads",
               "70B": "hidden 8192, ffn 28672, 64/8 heads"}
 GEMV_SOURCES = ["ternary_weight_quant_b300/csrc/tw_gemv_stream.cu", "ternary_weight_quant_b300/csrc/tw_common.cuh"]
-TRAFFIC_FILES = {"2b": os.path.join(ROOT, "profiles", "gemv_stream_2b_layer_launches.md")}
+TRAFFIC_FILES = {"2b": os.path.join(ROOT, "profiles", "gemv_decode_2b_layer_launches.md")}
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -867,7 +867,7 @@ def run_ours(args):
     # latency per call, a read-only streaming rate as a third bandwidth basis, and every other
     # configuration with its own roofline and CPU baseline
     extra = {}
-    default = args.workload == "2b" and not args.separate
+    default = args.workload == "2b" and not args.separate and not args.no_extras
     if default:
         ugraph = capture(stack, fused=False)
         for _ in range(args.warmup):
@@ -886,7 +886,7 @@ def run_ours(args):
     cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
     if default and cpu_ok:
         extra["small_case"]["cpu_oracle_us_per_call_single_thread"] = cpu_small_case_us()
-    if default and not args.no_workloads:
+    if default and not args.no_workloads:  # (--no-extras leaves `default` false)
         wl = {}
         for name in OTHER_WORKLOADS:
             r, st, gr, _ = measure(tw, name, args.workload_steps, 3, world)
@@ -950,10 +950,11 @@ def run_ours(args):
 def run_kernel_case(args):
     """Kernels in isolation (for timing sweeps and small ncu captures; not the contract line).
 
-    --kernel-case {gemv,t5,fused,fused_rms,quant,rms_quant,gemm,gemm_nows,matmul} (a comma list) on --shape
-    NxK at --M tokens (a comma list), over --copies distinct weight tensors (so the stream leaves
-    L2); one pass over them is captured in a CUDA graph and replayed --reps times (device time
-    per launch, host launch cost excluded).  One JSON line per (case, M)."""
+    --kernel-case {gemv,t5,fused,fused_rms,residual,stats,quant,rms_quant,gemm,gemm_nows,matmul}
+    (a comma list) on --shape NxK at --M tokens (a comma list), over --copies distinct weight
+    tensors (so the stream leaves L2); one pass over them is captured in a CUDA graph and
+    replayed --reps times (device time per launch, host launch cost excluded).  One JSON line
+    per (case, M).  residual and stats take one token."""
     import torch
     import seeded_inputs as si
     torch.cuda.set_device(0)
@@ -962,6 +963,7 @@ def run_kernel_case(args):
     ws = torch.empty(tw.tw_pack_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
     cases = args.kernel_case.split(",")
     packs, packs5 = [], []
+    epi_ws = tw.epilogue_workspace() if any(k in ("residual", "stats") for k in cases) else None
     for c in range(args.copies):
         W = si.device_normal((N, K), seed=77 + c)
         if any(k != "t5" for k in cases):
@@ -978,10 +980,23 @@ def run_kernel_case(args):
         xq, sx, xs = tw.quantize(x)
         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
         gws = tw.gemm_workspace(M, K)
+        if epi_ws is not None:
+            # residual case: the residual stream has N elements; stats case: x has K elements, and
+            # the partial statistics come from one residual call over K outputs first
+            hN = si.device_normal((N,), seed=11)
+            hK = si.device_normal((K,), seed=12)
+            gN = 1.0 + 0.1 * si.device_normal((N,), seed=13)
+            pKK = tw.pack(si.device_normal((K, K), seed=14))
+            xK = si.device_normal((1, K), seed=15)
+            tw.tw_quant_gemv_residual(xK, pKK[0], pKK[1], hK, hK, gain, epi_ws)
         for k in cases:
 
             def launch(p, g):
-                if k == "t5":
+                if k == "residual":
+                    tw.tw_quant_gemv_residual(x, p, g, hN, hN, gN, epi_ws, y=y)
+                elif k == "stats":
+                    tw.tw_quant_gemv_stats(hK, gain, epi_ws, p, g, y)
+                elif k == "t5":
                     tw.tw_ternary_gemv_t5(p, g, xq, sx, y)
                 elif k == "gemv":
                     tw.tw_ternary_gemv(p, g, xq, sx, y, xs)
@@ -1054,8 +1069,12 @@ def main():
     ap.add_argument("--no-workloads", action="store_true",
                     help="default run: leave out the other configurations")
     ap.add_argument("--workload-steps", type=int, default=10, help="timed steps of each other configuration")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default workload: skip the unfused step, small case, read stream, five-trit and "
+                         "epilogue measurements (and the other configurations)")
     ap.add_argument("--kernel-case", default=None,
-                    help="time one kernel alone: gemv, t5, fused, fused_rms, quant, rms_quant, gemm, gemm_nows or matmul")
+                    help="time one kernel alone: gemv, t5, fused, fused_rms, residual, stats, quant, rms_quant, gemm, "
+                         "gemm_nows or matmul")
     ap.add_argument("--shape", default="13824x2560", help="NxK for --kernel-case")
     ap.add_argument("--M", default="1", help="tokens for --kernel-case (a comma list)")
     ap.add_argument("--copies", type=int, default=8, help="distinct weight tensors for --kernel-case")
