@@ -185,10 +185,11 @@ TW_API tw_status tw_rmsnorm_quant_act(const float *x, const float *g, float eps,
  *   acc_out  [M][N] int32 output of the exact accumulators, or NULL.
  * Requires 1 <= M <= TW_GEMV_MAX_M, N >= 1, 4 <= K <= TW_MAX_K, K % 4 == 0.  The fast
  * paths need K % 64 == 0 and packed and x_q 16-byte aligned: up to 4 tokens the
- * streaming kernel (integer dp4a), from 5 to 16 the tensor cores through mma.sync with
- * f16 operands and fp32 accumulation, exact (the 2-bit codes enter as f16 bit patterns
- * c 4^s 2^-24, the activations scaled by 4^-s; every partial sum is a multiple of
- * 2^-24 below 1).  Other cases take a slower exact path (dp4a).
+ * streaming kernel (integer dp4a), from 5 to 16 -- and from 3 for rows of at most 8192
+ * weights that one CTA block per SM holds -- the tensor cores through mma.sync with f16
+ * operands and fp32 accumulation, exact (the 2-bit codes enter as f16 bit patterns
+ * c 4^s 2^-24, the activations scaled by 4^-s; every partial sum is a multiple of 2^-24
+ * below 1).  Other cases take a slower exact path (dp4a).
  */
 TW_API tw_status tw_ternary_gemv(const uint8_t *packed, const float *w_scale, const int8_t *x_q,
                                  const float *s_x, const int32_t *x_sum, int64_t M, int64_t N,
@@ -259,8 +260,8 @@ TW_API tw_status tw_ternary_gemm(const uint8_t *packed, const float *w_scale, co
 
 /*
  * The product for any M: tw_ternary_gemv below the measured crossover (M <= 16; M <= 11
- * for matrices of 2^24 weights or more with K >= 4096 when a large enough workspace is
- * given, K % 64 == 0),
+ * for matrices of 2^24 weights or more with K > 16384, or with N < 4096 and K >= 6912, when
+ * a large enough workspace is given, K % 64 == 0),
  * tw_ternary_gemm above it (when K % 16 == 0 and packed / x_q are 16-byte aligned; an
  * exact CUDA-core kernel otherwise).  Arguments as tw_ternary_gemm; the workspace is
  * used only on the tensor-core path and may be NULL.

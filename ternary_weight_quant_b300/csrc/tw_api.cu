@@ -37,6 +37,7 @@ cudaError_t tw_launch_fused_gemv(const float* x, const float* g, float eps, cons
                                  int num_sms, bool pdl);
 cudaError_t tw_read_stream_status(int* out);
 int tw_mma_supported(int M, int N, int K);
+int tw_mma_persistent(int M, int N, int K, int num_sms);
 cudaError_t tw_launch_gemv_mma(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
                                int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream,
                                int num_sms);
@@ -135,8 +136,14 @@ tw_status check_product_args(const uint8_t* packed, const float* w_scale, const 
 }  // namespace
 
 // Tokens from which tw_ternary_gemv takes the tensor-core (mma.sync) kernel (up to 16): below
-// it the integer product of the streaming kernel is cheaper than an 8-token tensor tile.
+// it the integer product of the streaming kernel is cheaper than an 8-token tensor tile.  At 3
+// and 4 tokens the mma.sync kernel still wins on rows of up to 8192 weights whose plan is one
+// block per CTA (measured on B300, us per call in a graph: 70B gate|up 57344 x 8192 at 4
+// tokens 75 against 126, 70B q|k|v 10240 x 8192 17 against 26, 2B gate|up 13824 x 2560 9.0
+// against 11.8; the streaming kernel at 4096 x 14336 13.7 against 18.7 and at the persistent
+// plan of 28672 x 4096 24.1 against 28.2).
 static const int64_t kMmaMinM = 5;
+static const int64_t kMmaMinMShortRows = 3;
 
 extern "C" {
 
@@ -235,7 +242,9 @@ TW_API tw_status tw_ternary_gemv(const uint8_t* packed, const float* w_scale, co
   if (st != TW_OK) return st;
   st = check_device_ptrs(packed, w_scale, x_q, s_x, x_sum, y, acc_out);
   if (st != TW_OK) return st;
-  if (M >= kMmaMinM && aligned(packed, 16) && aligned(x_q, 16) && tw_mma_supported((int)M, (int)N, (int)K))
+  const bool mma_m = M >= kMmaMinM ||
+                     (M >= kMmaMinMShortRows && K <= 8192 && !tw_mma_persistent((int)M, (int)N, (int)K, sms));
+  if (mma_m && aligned(packed, 16) && aligned(x_q, 16) && tw_mma_supported((int)M, (int)N, (int)K))
     return from_cuda(tw_launch_gemv_mma(packed, w_scale, x_q, s_x, (int)M, (int)N, (int)K, y, acc_out,
                                         (cudaStream_t)stream, sms));
   if (aligned(packed, 16) && aligned(x_q, 16) && tw_stream_supported((int)M, (int)N, (int)K, sms))
@@ -293,18 +302,21 @@ TW_API tw_status tw_ternary_gemm(const uint8_t* packed, const float* w_scale, co
 }
 
 // Token count from which the tcgen05 GEMM takes over from the GEMV kernels (the mma.sync
-// kernel from 5 to 16 tokens).  Measured on B300, microseconds per call chained in a graph:
-// 13824 x 2560 at 16 tokens 11.3 (mma.sync) against 18.0 (GEMM); 2560 x 6912 at 16 tokens
-// 18.9 against 14.7, and at 8 tokens 12.5 against 14.4.  So long rows (K >= 4096) of large
-// matrices (N K >= 2^24) go to the GEMM from 12 tokens when it can use its workspace.
+// kernel from 5 to 16 tokens).  Measured on B300, microseconds per call chained in a graph, at
+// 12 and 16 tokens (mma.sync against GEMM): 70B q|k|v 10240 x 8192 34.5 / 33.7 against 42.6 /
+// 42.8, 70B gate|up 57344 x 8192 141 against 150, 8B down 4096 x 14336 29.4 / 37.7 against
+// 43.5 / 43.7; but 70B down 8192 x 28672 (rows too long to stage) 75 / 83 against 69 and
+// 2560 x 6912 16.8 / 20.5 against 16.0 / 15.9.  So from 12 tokens the GEMM takes rows longer
+// than 16384 weights, and narrow matrices (N < 4096) with rows of 6912 or more, when it can
+// use its workspace; 17 tokens and more always go to the GEMM.
 static const int64_t kGemmCrossoverM = 17;
 static const int64_t kGemmCrossoverLargeM = 12;
 static const int64_t kLargeWeights = (int64_t)1 << 24;
 
 static bool prefer_gemm(int64_t M, int64_t N, int64_t K, const void* workspace, size_t ws_bytes) {
   if (M >= kGemmCrossoverM || M > TW_GEMV_MAX_M) return true;
-  return M >= kGemmCrossoverLargeM && K >= 4096 && N * K >= kLargeWeights && K % 64 == 0 &&
-         workspace != nullptr && ws_bytes >= tw_gemm_ws_size((int)M, (int)K);
+  return M >= kGemmCrossoverLargeM && (K > 16384 || (N < 4096 && K >= 6912)) && N * K >= kLargeWeights &&
+         K % 64 == 0 && workspace != nullptr && ws_bytes >= tw_gemm_ws_size((int)M, (int)K);
 }
 
 TW_API tw_status tw_ternary_matmul(const uint8_t* packed, const float* w_scale, const int8_t* x_q,

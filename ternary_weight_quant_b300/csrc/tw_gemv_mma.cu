@@ -25,13 +25,14 @@
 // lane q hold codes o0, o0 + 8, o1, o1 + 8 with o0 = 2q, o1 = 2q + 1, or 6 and 7 for q = 3);
 // B is gathered in the same order, so the sum is unchanged.
 //
-// Work split: a CTA owns TC consecutive tiles of 16 rows; its 8 warps are G groups x SL K
-// slices; group g takes tiles g, g + G, ... (up to TWM per warp), slice s a range of 64-k
-// steps.  The CTA's rows are first copied into shared memory by bulk copies, one per row into
+// Work split: a CTA owns blocks of TC consecutive tiles of 16 rows; its 8 warps are G groups
+// x SL K slices; group g takes tiles g, g + G, ... (up to TWM per warp), slice s a range of
+// 64-k steps.  A block's rows are copied into shared memory by bulk copies, one per row into
 // rows padded by 16 bytes (the eight rows a warp reads at once then fall in different
-// banks), all in flight together and completing on one mbarrier (bounded wait); without room
-// for them (SMEM = false) each warp loads its rows' words from global memory one group of
-// four 16-steps ahead.  A quad's four lanes share each 16-byte load.  The activations come
+// banks), all in flight together and completing on one mbarrier (bounded wait).  Small
+// matrices take one block per CTA; large ones a persistent grid with two buffers, the next
+// block's copies running under the current block's computation; without room for even one
+// tile each warp loads its rows' words from global memory one group of four 16-steps ahead.  A quad's four lanes share each 16-byte load.  The activations come
 // straight from global memory (x_q is small and stays in L1).  Slices meet in shared memory
 // through float atomics (exact: integer multiples of 2^-24 below 1).  Epilogue: per row and
 // token, the accumulator minus sum x_q, dequantised as everywhere else.
@@ -94,45 +95,71 @@ __device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t 
   return d;
 }
 
-// NT (1 or 2) n-tiles of 8 tokens (M <= 8 NT); TWM tiles of 16 rows per warp (TC = G * TWM);
-// SMEM: the CTA's rows are staged in shared memory.
-template <int NT, int TWM, bool SMEM>
+// NT (1 or 2) n-tiles of 8 tokens (M <= 8 NT); TWM tiles of 16 rows per warp (TC = G * TWM).
+// STAGE 0: rows read from global memory one group ahead; 1: the CTA's block of TC tiles is
+// staged in shared memory once; 2 (persistent): the CTA takes blocks blockIdx.x, + gridDim.x,
+// ... through two shared-memory buffers, the copies of block b + 2 issued as soon as block b
+// is computed, so that they run under the computation of block b + 1.
+template <int NT, int TWM, int STAGE>
 __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
   static_assert(NT == 1 || NT == 2, "8 or 16 tokens per kernel");
+  constexpr bool SMEM = STAGE > 0;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // [SL][TC][16][8 NT] partial sums of each K slice (units of 2^-24), summed in the epilogue
   float* dsum = reinterpret_cast<float*>(smem_raw);
-  unsigned char* wsm = smem_raw + (size_t)a.SL * a.TC * 16 * (8 * NT) * sizeof(float);  // SMEM: [TC*16][wrow]
+  unsigned char* wbase = smem_raw + (size_t)a.SL * a.TC * 16 * (8 * NT) * sizeof(float);  // [1 or 2][TC*16][wrow]
+  const size_t bufsz = (size_t)a.TC * 16 * a.wrow;
   __shared__ int xsum_s[8 * NT];
   __shared__ float cs_s[8 * NT];  // per token: the dequantisation scale fl(fl(gamma s_x) / 127)
-  __shared__ __align__(8) unsigned long long wbar;
+  __shared__ __align__(8) unsigned long long wbar[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane & 3, rq = lane >> 2;
   const int MP = 8 * NT;
   const int K = a.K, Kw = K >> 4, T4 = K >> 6;  // 16-steps (words) per row, groups of four
   const int g = warp / a.SL, sl = warp % a.SL;
-  const int tile0 = blockIdx.x * a.TC;
   const int ntiles_all = (a.N + 15) >> 4;
+  const int nblk_all = (ntiles_all + a.TC - 1) / a.TC;
+  const uint32_t rb = (uint32_t)(K >> 2);
+
+  // warp 0: the rows of block blk into buffer buf, all copies completing on wbar[buf]: one
+  // bulk copy per row into padded rows, or (unpadded, wrow = K / 4) the block's contiguous
+  // bytes in pieces of up to 32 KB
+  auto issue = [&](int blk, int buf) {
+    const int rows = min(a.TC * 16, a.N - blk * a.TC * 16);
+    const uint32_t bar = smem_u32(&wbar[buf]);
+    const uint32_t total = (uint32_t)rows * rb;
+    if (lane == 0)
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(total) : "memory");
+    __syncwarp();
+    unsigned char* dst = wbase + (size_t)buf * bufsz;
+    const unsigned char* src = a.packed + (size_t)blk * a.TC * 16 * rb;
+    if ((uint32_t)a.wrow == rb) {
+      for (uint32_t off = 32768u * (uint32_t)lane; off < total; off += 32768u * 32u)
+        asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_u32(dst + off)),
+                     "l"(src + off), "r"(min(32768u, total - off)), "r"(bar)
+                     : "memory");
+    } else {
+      for (int r = lane; r < rows; r += 32)
+        asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_u32(dst + (size_t)r * a.wrow)),
+                     "l"(src + (size_t)r * rb), "r"(rb), "r"(bar)
+                     : "memory");
+    }
+  };
 
   // programmatic dependent launch: the weights are parameters and are fetched at once; the
   // activations, their scales and the outputs belong to the previous kernel until the wait
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const uint32_t bar = smem_u32(&wbar);
-  if (SMEM && warp == 0) {  // the CTA's rows, one bulk copy per row, all on one mbarrier
-    const int rows = min(a.TC * 16, a.N - tile0 * 16);
-    const uint32_t rb = (uint32_t)(K >> 2);
+  if (SMEM && warp == 0) {
     if (lane == 0) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar[0])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar[1])) : "memory");
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"((uint32_t)rows * rb)
-                   : "memory");
     }
     __syncwarp();
-    for (int r = lane; r < rows; r += 32)
-      asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                       smem_u32(wsm + (size_t)r * a.wrow)),
-                   "l"(a.packed + ((size_t)tile0 * 16 + r) * rb), "r"(rb), "r"(bar)
-                   : "memory");
+    if (blockIdx.x < nblk_all) issue(blockIdx.x, 0);
+    if (STAGE == 2 && blockIdx.x + gridDim.x < nblk_all) issue(blockIdx.x + gridDim.x, 1);
   }
   const float gam = __ldg(a.w_scale);
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -156,37 +183,41 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
   const int xw_lo = q < 2 ? 0 : 1;
   const uint32_t xsel = (q & 1) ? 0x7362u : 0x5140u;
 
-  // this warp's tiles and K range (in groups of four 16-steps)
+  // this warp's K range (in groups of four 16-steps)
   const int gs = (T4 + a.SL - 1) / a.SL;
   const int g0 = sl * gs, g1 = min(T4, g0 + gs);
   const uint32_t* W = reinterpret_cast<const uint32_t*>(a.packed);
   const uint32_t* X = reinterpret_cast<const uint32_t*>(a.x_q);
-
-  int rowA[TWM], rowB[TWM];  // rows rq and rq + 8 of each tile (clamped into the matrix)
-#pragma unroll
-  for (int i = 0; i < TWM; ++i) {
-    const int tile = min(tile0 + g + i * a.G, ntiles_all - 1);
-    rowA[i] = min(tile * 16 + rq, a.N - 1);
-    rowB[i] = min(tile * 16 + rq + 8, a.N - 1);
-    if (SMEM) {  // as rows of the CTA's staged block
-      rowA[i] -= tile0 * 16;
-      rowB[i] -= tile0 * 16;
-    }
-  }
-  float acc[TWM][NT][4];
-#pragma unroll
-  for (int i = 0; i < TWM; ++i)
-#pragma unroll
-    for (int n = 0; n < NT; ++n) acc[i][n][0] = acc[i][n][1] = acc[i][n][2] = acc[i][n][3] = 0.0f;
   int xs_lane[NT];
 #pragma unroll
   for (int n = 0; n < NT; ++n) xs_lane[n] = 0;
 
-  uint4 wa[TWM], wb[TWM];  // words of the current group (four 16-steps) for rows A and B
-  auto load_w = [&](int gi) {
+  int b = 0;
+  for (int blk = blockIdx.x; blk < nblk_all; blk += gridDim.x, ++b) {
+    const int tile0 = blk * a.TC;
+    const int buf = STAGE == 2 ? (b & 1) : 0;
+    const unsigned char* wsm = wbase + (size_t)buf * bufsz;
+    int rowA[TWM], rowB[TWM];  // rows rq and rq + 8 of each tile (clamped into the matrix)
 #pragma unroll
     for (int i = 0; i < TWM; ++i) {
-      {
+      const int tile = min(tile0 + g + i * a.G, ntiles_all - 1);
+      rowA[i] = min(tile * 16 + rq, a.N - 1);
+      rowB[i] = min(tile * 16 + rq + 8, a.N - 1);
+      if (SMEM) {  // as rows of the staged block
+        rowA[i] -= tile0 * 16;
+        rowB[i] -= tile0 * 16;
+      }
+    }
+    float acc[TWM][NT][4];
+#pragma unroll
+    for (int i = 0; i < TWM; ++i)
+#pragma unroll
+      for (int n = 0; n < NT; ++n) acc[i][n][0] = acc[i][n][1] = acc[i][n][2] = acc[i][n][3] = 0.0f;
+
+    uint4 wa[TWM], wb[TWM];  // words of the current group (four 16-steps) for rows A and B
+    auto load_w = [&](int gi) {
+#pragma unroll
+      for (int i = 0; i < TWM; ++i) {
         if (SMEM) {
           wa[i] = *reinterpret_cast<const uint4*>(wsm + (size_t)rowA[i] * a.wrow + 16 * gi);
           wb[i] = *reinterpret_cast<const uint4*>(wsm + (size_t)rowB[i] * a.wrow + 16 * gi);
@@ -195,101 +226,111 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
           wb[i] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)rowB[i] * Kw) + gi);
         }
       }
-    }
-  };
-  bool ok = true;
-  if (SMEM) {  // warp-uniform: a warp gives up as a whole (outputs then left unwritten)
-    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, 0));
-    if (!ok && lane == 0) atomicCAS(&g_mma_status, 0, (int)TW_ERR_TIMEOUT);
-  }
-  if (ok && g0 < g1) load_w(g0);
-  for (int gi = ok ? g0 : g1; gi < g1; ++gi) {
-    uint4 ca[TWM], cb[TWM];
-#pragma unroll
-    for (int i = 0; i < TWM; ++i) {
-      ca[i] = wa[i];
-      cb[i] = wb[i];
-    }
-    if (gi + 1 < g1) load_w(gi + 1);  // the next group's words are in flight during this one
-    // B for token n * 8 + rq: this lane's four activations x[o0], x[o0 + 8], x[o1], x[o1 + 8]
-    // of a 16-step, scaled and in f16 (tokens past M: x = 0).  Plain loads: x_q was written by
-    // the previous kernel (read after the dependency wait).
-    auto make_b = [&](uint32_t lo, uint32_t hi, int n, uint32_t& b0, uint32_t& b1) {
-      const uint32_t xb = __byte_perm(lo, hi, xsel);
-      if (n * 8 + rq < a.M) xs_lane[n] = __dp4a((int)xb, 0x01010101, xs_lane[n]);
-      const uint32_t u = xb ^ 0x80808080u;  // x + 128 as bytes
-      b0 = hfma2_bits(__byte_perm(u, 0x6464u, 0x4140u), sc0, nb0);
-      b1 = hfma2_bits(__byte_perm(u, 0x6464u, 0x4342u), sc1, nb1);
     };
-    auto x_words = [&](int n) -> const uint32_t* {
-      return X + ((size_t)min(n * 8 + rq, a.M - 1) * K >> 2) + 16 * gi;
-    };
-    // the group's activation words all at once, then four 16-steps
-    uint32_t xlo[4][NT], xhi[4][NT];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const uint32_t* xp = x_words(n);
-      const bool in = n * 8 + rq < a.M;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        xlo[s][n] = in ? xp[4 * s + xw_lo] : 0u;
-        xhi[s][n] = in ? xp[4 * s + xw_lo + 2] : 0u;
-      }
+    bool ok = true;
+    if (SMEM) {  // warp-uniform: a warp gives up as a whole (outputs then left unwritten)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&wbar[buf]), STAGE == 2 ? (uint32_t)((b >> 1) & 1) : 0u));
+      if (!ok && lane == 0) atomicCAS(&g_mma_status, 0, (int)TW_ERR_TIMEOUT);
     }
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      uint32_t b0[NT], b1[NT];
-#pragma unroll
-      for (int n = 0; n < NT; ++n) make_b(xlo[s][n], xhi[s][n], n, b0[n], b1[n]);
+    if (ok && g0 < g1) load_w(g0);
+    for (int gi = ok ? g0 : g1; gi < g1; ++gi) {
+      uint4 ca[TWM], cb[TWM];
 #pragma unroll
       for (int i = 0; i < TWM; ++i) {
-        const uint32_t w_a = (s == 0 ? ca[i].x : s == 1 ? ca[i].y : s == 2 ? ca[i].z : ca[i].w) >> sh;
-        const uint32_t w_b = (s == 0 ? cb[i].x : s == 1 ? cb[i].y : s == 2 ? cb[i].z : cb[i].w) >> sh;
+        ca[i] = wa[i];
+        cb[i] = wb[i];
+      }
+      if (gi + 1 < g1) load_w(gi + 1);  // the next group's words are in flight during this one
+      // B for token n * 8 + rq: this lane's four activations x[o0], x[o0 + 8], x[o1], x[o1 + 8]
+      // of a 16-step, scaled and in f16 (tokens past M: x = 0).  Plain loads: x_q was written by
+      // the previous kernel (read after the dependency wait).  Sums of x_q: first block only.
+      auto make_b = [&](uint32_t lo, uint32_t hi, int n, uint32_t& b0, uint32_t& b1) {
+        const uint32_t xb = __byte_perm(lo, hi, xsel);
+        if (b == 0 && n * 8 + rq < a.M) xs_lane[n] = __dp4a((int)xb, 0x01010101, xs_lane[n]);
+        const uint32_t u = xb ^ 0x80808080u;  // x + 128 as bytes
+        b0 = hfma2_bits(__byte_perm(u, 0x6464u, 0x4140u), sc0, nb0);
+        b1 = hfma2_bits(__byte_perm(u, 0x6464u, 0x4342u), sc1, nb1);
+      };
+      // the group's activation words all at once, then four 16-steps
+      uint32_t xlo[4][NT], xhi[4][NT];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) mma_f16(acc[i][n], w_a & m0, w_b & m0, w_a & m1, w_b & m1, b0[n], b1[n]);
+      for (int n = 0; n < NT; ++n) {
+        const uint32_t* xp = X + ((size_t)min(n * 8 + rq, a.M - 1) * K >> 2) + 16 * gi;
+        const bool in = n * 8 + rq < a.M;
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          xlo[s4][n] = in ? xp[4 * s4 + xw_lo] : 0u;
+          xhi[s4][n] = in ? xp[4 * s4 + xw_lo + 2] : 0u;
+        }
+      }
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        uint32_t b0[NT], b1[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) make_b(xlo[s4][n], xhi[s4][n], n, b0[n], b1[n]);
+#pragma unroll
+        for (int i = 0; i < TWM; ++i) {
+          const uint32_t w_a = (s4 == 0 ? ca[i].x : s4 == 1 ? ca[i].y : s4 == 2 ? ca[i].z : ca[i].w) >> sh;
+          const uint32_t w_b = (s4 == 0 ? cb[i].x : s4 == 1 ? cb[i].y : s4 == 2 ? cb[i].z : cb[i].w) >> sh;
+#pragma unroll
+          for (int n = 0; n < NT; ++n) mma_f16(acc[i][n], w_a & m0, w_b & m0, w_a & m1, w_b & m1, b0[n], b1[n]);
+        }
       }
     }
-  }
 
-  // each slice's partial sums to its own slot: D[row][token] of tile i is (c0, c1) at row rq,
-  // tokens 2q, 2q + 1 and (c2, c3) at row rq + 8
+    // each slice's partial sums to its own slot: D[row][token] of tile i is (c0, c1) at row rq,
+    // tokens 2q, 2q + 1 and (c2, c3) at row rq + 8
 #pragma unroll
-  for (int i = 0; i < TWM; ++i) {
-    float* d = dsum + ((size_t)sl * a.TC + g + i * a.G) * 16 * MP;
+    for (int i = 0; i < TWM; ++i) {
+      float* d = dsum + ((size_t)sl * a.TC + g + i * a.G) * 16 * MP;
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int tk = n * 8 + 2 * q;
-      *reinterpret_cast<float2*>(&d[rq * MP + tk]) = make_float2(ok ? acc[i][n][0] : 0.f, ok ? acc[i][n][1] : 0.f);
-      *reinterpret_cast<float2*>(&d[(rq + 8) * MP + tk]) = make_float2(ok ? acc[i][n][2] : 0.f, ok ? acc[i][n][3] : 0.f);
+      for (int n = 0; n < NT; ++n) {
+        const int tk = n * 8 + 2 * q;
+        *reinterpret_cast<float2*>(&d[rq * MP + tk]) = make_float2(ok ? acc[i][n][0] : 0.f, ok ? acc[i][n][1] : 0.f);
+        *reinterpret_cast<float2*>(&d[(rq + 8) * MP + tk]) =
+            make_float2(ok ? acc[i][n][2] : 0.f, ok ? acc[i][n][3] : 0.f);
+      }
     }
-  }
-  // sum of x_q per token: the slices of group 0 cover K once; a quad covers a 16-group
-  if (g == 0) {
+    // sum of x_q per token: the slices of group 0 cover K once; a quad covers a 16-group
+    if (b == 0 && g == 0) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      int v = xs_lane[n];
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      if (q == 0 && n * 8 + rq < a.M) atomicAdd(&xsum_s[n * 8 + rq], v);
+      for (int n = 0; n < NT; ++n) {
+        int v = xs_lane[n];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (q == 0 && n * 8 + rq < a.M) atomicAdd(&xsum_s[n * 8 + rq], v);
+      }
     }
-  }
-  if (__syncthreads_or(!ok)) {  // a bounded wait gave up: no outputs; the copies must land first
-    if (SMEM) mbar_wait_bounded(bar, 0);
-    return;
-  }
+    if (__syncthreads_or(!ok)) {  // a bounded wait gave up: no more outputs; copies must land first
+      if (SMEM) {
+        mbar_wait_bounded(smem_u32(&wbar[buf]), STAGE == 2 ? (uint32_t)((b >> 1) & 1) : 0u);
+        if (STAGE == 2 && blk + gridDim.x < nblk_all)  // the other buffer's block was issued too
+          mbar_wait_bounded(smem_u32(&wbar[buf ^ 1]), (uint32_t)(((b + 1) >> 1) & 1));
+      }
+      return;
+    }
+    // this buffer is free again (every warp has passed the barrier above, so its reads are
+    // done): its next block starts loading under the next computation
+    if (STAGE == 2 && warp == 0 && blk + 2 * (int)gridDim.x < nblk_all) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(blk + 2 * gridDim.x, buf);
+    }
 
-  const size_t slot = (size_t)a.TC * 16 * MP;
-  for (int i = tid; i < a.TC * 16 * MP; i += kThreads) {
-    const int tk = i % MP, r = i / MP;
-    const int row = tile0 * 16 + r;
-    if (tk >= a.M || row >= a.N) continue;
-    float d = 0.0f;  // exact: multiples of 2^-24 below 1
-    for (int k = 0; k < a.SL; ++k) d += dsum[k * slot + i];
-    // 2^24 times a multiple of 2^-24 below 1: an exact integer
-    const int acc_i = __float2int_rn(__fmul_rn(d, 16777216.0f)) - xsum_s[tk];
-    const size_t o = (size_t)tk * a.N + row;
-    a.y[o] = dequant(acc_i, cs_s[tk], gam, a.s_x[tk]);
-    if (a.acc_out) a.acc_out[o] = acc_i;
+    const size_t slot = (size_t)a.TC * 16 * MP;
+    for (int i = tid; i < a.TC * 16 * MP; i += kThreads) {
+      const int tk = i % MP, r = i / MP;
+      const int row = tile0 * 16 + r;
+      if (tk >= a.M || row >= a.N) continue;
+      float d = 0.0f;  // exact: multiples of 2^-24 below 1
+      for (int k = 0; k < a.SL; ++k) d += dsum[k * slot + i];
+      // 2^24 times a multiple of 2^-24 below 1: an exact integer
+      const int acc_i = __float2int_rn(__fmul_rn(d, 16777216.0f)) - xsum_s[tk];
+      const size_t o = (size_t)tk * a.N + row;
+      a.y[o] = dequant(acc_i, cs_s[tk], gam, a.s_x[tk]);
+      if (a.acc_out) a.acc_out[o] = acc_i;
+    }
+    if (STAGE < 2) break;
+    __syncthreads();  // dsum is written again by the next block
   }
 }
 
@@ -298,9 +339,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
 
 namespace {
 
-template <int NT, int TWM, bool SMEM>
+template <int NT, int TWM, int STAGE>
 cudaError_t launch_mma(const tw::mma::Args& a, size_t smem, int grid, cudaStream_t stream) {
-  auto kern = tw::mma::gemv_mma_kernel<NT, TWM, SMEM>;
+  auto kern = tw::mma::gemv_mma_kernel<NT, TWM, STAGE>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -318,22 +359,22 @@ cudaError_t launch_mma(const tw::mma::Args& a, size_t smem, int grid, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int NT, bool SMEM>
+template <int NT, int STAGE>
 cudaError_t launch_mma_tw(const tw::mma::Args& a, int tw, size_t smem, int grid, cudaStream_t stream) {
   if constexpr (NT == 1) {
-    if (tw == 4) return launch_mma<NT, 4, SMEM>(a, smem, grid, stream);
+    if (tw == 4) return launch_mma<NT, 4, STAGE>(a, smem, grid, stream);
   }
   if constexpr (NT <= 2) {
-    if (tw == 3) return launch_mma<NT, 3, SMEM>(a, smem, grid, stream);
+    if (tw == 3) return launch_mma<NT, 3, STAGE>(a, smem, grid, stream);
   }
-  if (tw == 2) return launch_mma<NT, 2, SMEM>(a, smem, grid, stream);
-  return launch_mma<NT, 1, SMEM>(a, smem, grid, stream);
+  if (tw == 2) return launch_mma<NT, 2, STAGE>(a, smem, grid, stream);
+  return launch_mma<NT, 1, STAGE>(a, smem, grid, stream);
 }
 
 template <int NT>
-cudaError_t launch_mma_nt(const tw::mma::Args& a, int tw, size_t smem, int grid, bool staged, cudaStream_t stream) {
-  return staged ? launch_mma_tw<NT, true>(a, tw, smem, grid, stream)
-                : launch_mma_tw<NT, false>(a, tw, smem, grid, stream);
+cudaError_t launch_mma_nt(const tw::mma::Args& a, int tw, size_t smem, int grid, int stage, cudaStream_t stream) {
+  if (stage == 2) return launch_mma_tw<NT, 2>(a, tw, smem, grid, stream);
+  return stage == 1 ? launch_mma_tw<NT, 1>(a, tw, smem, grid, stream) : launch_mma_tw<NT, 0>(a, tw, smem, grid, stream);
 }
 
 // Shared memory a CTA may use: two CTAs per SM.
@@ -344,42 +385,97 @@ constexpr size_t kMmaSmemMax = 110 * 1024;
 // 1 when the tensor-core GEMV takes (M, N, K): 1 <= M <= 16, K % 64 == 0.
 int tw_mma_supported(int M, int N, int K) { return (M >= 1 && M <= 16 && N >= 1 && K % 64 == 0) ? 1 : 0; }
 
-// Launch plan: about two CTAs per SM; tiles per CTA TC, split into G groups (tiles per warp
-// at most 4 or 3 for 8 or 16 tokens: the accumulators are registers) and SL = 8 / G
-// slices of K (more slices when a CTA has few tiles); fewer tiles per CTA when its rows would
-// not fit in shared memory, and the unstaged kernel when not even one tile does.
-cudaError_t tw_launch_gemv_mma(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
-                               int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream,
-                               int num_sms) {
-  if (!tw_mma_supported(M, N, K)) return cudaErrorInvalidValue;
+// G groups of tiles: one while a warp can take all TC tiles (each warp forms the activation
+// operand once per 16-step for all its tiles, so more tiles per warp share that work), else
+// a power of two dividing TC, at most kWarps.
+static void split_groups(int TC, int twmax, int& G) {
+  G = 1;
+  if (TC <= twmax) return;
+  while (G * 2 <= tw::mma::kWarps && TC % (G * 2) == 0) G *= 2;
+}
+
+// Launch plan.  One block of TC tiles per CTA, about two CTAs per SM, staged in shared memory
+// when it fits (else read from global memory); tiles per CTA split into G groups (at most 4
+// or 3 tiles per warp for 8 or 16 tokens: the accumulators are registers) and SL = 8 / G
+// slices of K.  When that takes more than one wave of CTAs, a persistent grid instead walks
+// through the blocks with two shared-memory buffers (two CTAs per SM when both buffers fit in
+// kMmaSmemMax, else one CTA with up to twice that), loading one block while computing another.
+namespace {
+struct MmaPlan {
+  int NT, TC, G, grid, stage;
+  size_t wrow;
+};
+
+MmaPlan make_mma_plan(int M, int N, int K, int num_sms) {
   const int NT = M <= 8 ? 1 : 2;  // n-tiles of 8 tokens
   const int twmax = NT == 1 ? 4 : 3;
   const int tiles = (N + 15) / 16;
   const int target = 2 * num_sms;
   const size_t wrow = (size_t)K / 4 + 16;
+  const size_t dsum_tile = (size_t)tw::mma::kWarps * 16 * (8 * NT) * sizeof(float);  // up to 8 slices
   // rows + partial sums of up to 8 slices
-  const size_t tile_bytes = 16 * wrow + (size_t)tw::mma::kWarps * 16 * (8 * NT) * sizeof(float);
+  const size_t tile_bytes = 16 * wrow + dsum_tile;
   const int fit = (int)(kMmaSmemMax / tile_bytes);
-  const bool staged = fit >= 1;
+  int stage = fit >= 1 ? 1 : 0;
   int TC = (tiles + target - 1) / target;
-  if (staged && TC > fit) TC = fit;
-  // G groups of TW tiles per warp, G dividing TC (every warp the same number of tiles)
-  int G = 1;
-  while (G * 2 <= tw::mma::kWarps && TC % (G * 2) == 0) G *= 2;
+  if (stage && TC > fit) TC = fit;
+  int G;
+  split_groups(TC, twmax, G);
   while (TC / G > twmax) {  // too many tiles per warp: fewer tiles per CTA, more CTAs
     TC -= 1;
-    G = 1;
-    while (G * 2 <= tw::mma::kWarps && TC % (G * 2) == 0) G *= 2;
+    split_groups(TC, twmax, G);
   }
-  const int grid = (tiles + TC - 1) / TC;
+  int grid = (tiles + TC - 1) / TC;
+  size_t wrow_used = wrow;
+  // More than one wave of CTAs: the persistent double-buffered plan, where it measured faster
+  // than one block per CTA (rows of up to 4096 weights, or 16 tokens).  Two CTAs per SM
+  // within kMmaSmemMax each, or one with twice that: the one that gives a warp more tiles
+  // (one tile per warp repeats the activation operand's work for every 256 weights); ties:
+  // two CTAs.
+  if (grid > target && (K <= 4096 || NT == 2)) {
+    const size_t wr = (size_t)K / 4;  // unpadded: one contiguous copy per block
+    int best_tw = 0;
+    for (int cps = 2; cps >= 1; --cps) {
+      const size_t budget = cps == 2 ? kMmaSmemMax : 2 * kMmaSmemMax;
+      int tc = (int)(budget / (2 * 16 * wr + dsum_tile));
+      if (tc < 1) continue;
+      if (tc > twmax) tc = twmax;  // one group: every warp takes all tiles of its K slice
+      if (tc <= best_tw) continue;
+      best_tw = tc;
+      const int nblk = (tiles + tc - 1) / tc;
+      stage = 2;
+      TC = tc;
+      G = 1;
+      grid = nblk < cps * num_sms ? nblk : cps * num_sms;
+      wrow_used = wr;
+    }
+  }
+  MmaPlan p;
+  p.NT = NT; p.TC = TC; p.G = G; p.grid = grid; p.stage = stage; p.wrow = wrow_used;
+  return p;
+}
+}  // namespace
+
+// 1 when the launch plan of (M, N, K) is the persistent double-buffered one.
+int tw_mma_persistent(int M, int N, int K, int num_sms) {
+  if (!tw_mma_supported(M, N, K)) return 0;
+  return make_mma_plan(M, N, K, num_sms).stage == 2 ? 1 : 0;
+}
+
+cudaError_t tw_launch_gemv_mma(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
+                               int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream,
+                               int num_sms) {
+  if (!tw_mma_supported(M, N, K)) return cudaErrorInvalidValue;
+  const MmaPlan p = make_mma_plan(M, N, K, num_sms);
   tw::mma::Args a = {};
   a.packed = packed; a.w_scale = w_scale; a.x_q = x_q; a.s_x = s_x;
-  a.M = M; a.N = N; a.K = K; a.TC = TC; a.G = G; a.SL = tw::mma::kWarps / G; a.wrow = (int)wrow;
+  a.M = M; a.N = N; a.K = K; a.TC = p.TC; a.G = p.G; a.SL = tw::mma::kWarps / p.G; a.wrow = (int)p.wrow;
   a.y = y; a.acc_out = acc_out;
-  const size_t smem = (size_t)a.SL * TC * 16 * (8 * NT) * sizeof(float) + (staged ? (size_t)TC * 16 * wrow : 0);
-  const int tw = TC / G;
-  return NT == 1 ? launch_mma_nt<1>(a, tw, smem, grid, staged, stream)
-                 : launch_mma_nt<2>(a, tw, smem, grid, staged, stream);
+  const size_t smem = (size_t)a.SL * p.TC * 16 * (8 * p.NT) * sizeof(float) +
+                      (size_t)(p.stage == 2 ? 2 : p.stage) * p.TC * 16 * p.wrow;
+  const int tw = p.TC / p.G;
+  return p.NT == 1 ? launch_mma_nt<1>(a, tw, smem, p.grid, p.stage, stream)
+                   : launch_mma_nt<2>(a, tw, smem, p.grid, p.stage, stream);
 }
 
 // Reads and clears the tensor-core GEMV's device status word (synchronous; diagnostics only).

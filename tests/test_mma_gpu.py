@@ -55,13 +55,13 @@ def check(y, acc, y_ref, acc_ref):
 
 @pytest.mark.parametrize("N,K", [(37, 64), (100, 2560), (640, 6912), (3840, 2560)])
 def test_mma_every_token_count(tw, N, K):
-    """5 .. 16 tokens through tw_ternary_gemv (the mma.sync kernel), 5 .. 64 through
-    tw_ternary_matmul (which hands 17 tokens and more to the tcgen05 GEMM)."""
+    """1 .. 16 tokens through tw_ternary_gemv (the mma.sync kernel from 5, and from 3 on the
+    shorter rows), 1 .. 64 through tw_ternary_matmul (17 tokens and more: the tcgen05 GEMM)."""
     W, x = si.gemv_case(64, N, K, seed=N + K, outliers=True)
     packed, gamma = oracle.pack_ternary(W)
     xq_all, sx_all, _ = oracle.quant_act(x)  # per token: the first M tokens are the M-token case
     y_all, acc_all = oracle.ternary_matmul(packed, gamma, xq_all, sx_all, openmp=True)
-    for M in range(5, 65):
+    for M in range(1, 65):
         xq, sx, y_ref, acc_ref = xq_all[:M], sx_all[:M], y_all[:M], acc_all[:M]
         if M <= 16:
             check(*run(tw, "tw_ternary_gemv", packed, gamma, xq, sx), y_ref, acc_ref)
@@ -69,11 +69,26 @@ def test_mma_every_token_count(tw, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(8, 13824, 2560), (16, 2560, 6912), (16, 6912, 2560), (13, 5000, 1024),
-                                   (9, 17, 12800), (16, 1, 64), (5, 3000, 40000)])
+                                   (9, 17, 12800), (16, 1, 64), (5, 3000, 40000), (3, 10240, 8192),
+                                   (4, 6144, 4096)])
 def test_mma_layer_shapes_and_plans(tw, M, N, K):
     """Shapes that take every launch plan: many tiles per CTA (groups of tiles), few tiles
     (K slices), a single row, tiles that end past N."""
     W, x = si.gemv_case(M, N, K, seed=M * 7 + N, outliers=True)
+    packed, gamma = oracle.pack_ternary(W)
+    xq, sx, _ = oracle.quant_act(x)
+    y_ref, acc_ref = oracle.ternary_matmul(packed, gamma, xq, sx, openmp=True)
+    check(*run(tw, "tw_ternary_gemv", packed, gamma, xq, sx), y_ref, acc_ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 30000, 4096), (16, 30000, 4096), (5, 6000, 14336), (12, 6000, 14336),
+                                   (7, 20011, 1024)])
+def test_mma_persistent_double_buffered(tw, M, N, K):
+    """Matrices with more row blocks than one wave of CTAs: the persistent plan, each CTA
+    loading its next block into one buffer while it computes from the other (two CTAs per
+    SM at K = 4096; one CTA with a larger budget at K = 14336, where two buffers of one tile
+    do not fit twice; a ragged last block at N = 20011)."""
+    W, x = si.gemv_case(M, N, K, seed=M + N + K, outliers=True)
     packed, gamma = oracle.pack_ternary(W)
     xq, sx, _ = oracle.quant_act(x)
     y_ref, acc_ref = oracle.ternary_matmul(packed, gamma, xq, sx, openmp=True)
