@@ -371,6 +371,16 @@ TW_API tw_status tw_ternary_gemv_t5(const uint8_t *packed5, const float *w_scale
  */
 TW_API tw_status tw_device_status(int32_t *status);
 
+/*
+ * Test switch for the failure handling of the tensor-core GEMM (diagnostics; synchronises
+ * the current device).  With on != 0, every tw_ternary_gemm launch that follows on this
+ * device starts with its abort flag raised, as if one of its bounded waits had given up
+ * before it issued any copy or product: it releases its tensor memory, waits for nothing
+ * that is not in flight, writes no output and records TW_ERR_TIMEOUT for tw_device_status.
+ * on = 0 restores normal operation.  No other call is affected.
+ */
+TW_API tw_status tw_debug_gemm_abort(int on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -53,6 +53,7 @@ def _load():
         "tw_epilogue_workspace_bytes": ([], sz),
         "tw_quant_gemv_residual": ([p, p, ctypes.c_float, p, p, i64, i64, p, p, p, p, p, p, sz, p], ctypes.c_int),
         "tw_quant_gemv_stats": ([p, p, ctypes.c_float, p, p, p, i64, i64, p, p, p, p, p, p], ctypes.c_int),
+        "tw_debug_gemm_abort": ([ctypes.c_int], ctypes.c_int),
         "tw_t5_row_bytes": ([i64], sz),
         "tw_pack_ternary_t5": ([p, i64, i64, p, p, p, sz, p], ctypes.c_int),
         "tw_ternary_gemv_t5": ([p, p, p, p, i64, i64, i64, p, p, p], ctypes.c_int),

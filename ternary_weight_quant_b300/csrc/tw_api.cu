@@ -42,6 +42,7 @@ cudaError_t tw_launch_gemv_mma(const uint8_t* packed, const float* w_scale, cons
                                int M, int N, int K, float* y, int32_t* acc_out, cudaStream_t stream,
                                int num_sms);
 cudaError_t tw_read_gemm_status(int* out);
+cudaError_t tw_set_gemm_abort_test(int on);
 cudaError_t tw_read_mma_status(int* out);
 cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const int8_t* x_q, const float* s_x,
                            int M, int N, int K, float* y, int32_t* acc_out, void* workspace, cudaStream_t stream,
@@ -420,6 +421,17 @@ TW_API tw_status tw_quant_gemv_stats(const float* x, const float* g, float eps, 
   if (st != TW_OK) return st;
   return from_cuda(tw_launch_quant_gemv_stats(x, g, eps, workspace, packed, w_scale, (int)N, (int)K, y, x_q_out,
                                               s_x_out, x_sum_out, acc_out, (cudaStream_t)stream, sms, true));
+}
+
+TW_API tw_status tw_debug_gemm_abort(int on) {
+  int sms = 0;
+  tw_status st = device_info(&sms);
+  if (st != TW_OK) return st;
+  if (tw_set_gemm_abort_test(on) != cudaSuccess) {
+    cudaGetLastError();
+    return TW_ERR_CUDA;
+  }
+  return TW_OK;
 }
 
 TW_API tw_status tw_device_status(int32_t* status) {

@@ -42,6 +42,10 @@ namespace tw {
 namespace gemm {
 
 __device__ int g_gemm_status;  // 0 or TW_ERR_TIMEOUT (sticky until read)
+// Diagnostic switch (tw_debug_gemm_abort): when set, every GEMM launch starts with its abort
+// flag raised, so it takes the path of a bounded wait that gave up before it issues any
+// copy or product.
+__device__ int g_gemm_abort_test;
 
 constexpr int BM = 128;            // weight rows per CTA (MMA M)
 constexpr int BK = 64;             // k per stage: one 128-byte swizzle row of bf16
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_done, 1);
-    *abort_flag = 0;
+    *abort_flag = g_gemm_abort_test;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 4) {
@@ -589,7 +593,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_init(op_empty + 8 * s, 1);
     }
     mbar_init(bar_done, 1);
-    *abort_flag = 0;
+    *abort_flag = g_gemm_abort_test;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 9) {
@@ -898,7 +902,7 @@ __global__ void __launch_bounds__(kTokThreads, 1)
       mbar_init(b_empty + 8 * s, 1);
     }
     mbar_init(bar_done, 1);
-    *abort_flag = 0;
+    *abort_flag = g_gemm_abort_test;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 9) {
@@ -1287,6 +1291,12 @@ cudaError_t tw_launch_gemm(const uint8_t* packed, const float* w_scale, const in
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, a);
+}
+
+// Sets the GEMM's abort test switch (synchronous; diagnostics only).
+cudaError_t tw_set_gemm_abort_test(int on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(tw::gemm::g_gemm_abort_test, &v, sizeof(int));
 }
 
 // Reads and clears the GEMM's device status word (synchronous; diagnostics only).
