@@ -17,8 +17,10 @@ offline).  The launches of a step are captured in one CUDA graph.
 
 value   = algorithmic bytes of all GEMVs in the step (packed weights + int8 activations
           + scales) / device time of the step, whole job (all ranks).
-e2e     = the same metric with the step's inputs copied from pinned host memory and all
-          outputs copied back inside the timed region (one copy each way).
+e2e     = the same metric with each step's inputs copied from pinned host memory and all its
+          outputs copied back inside the timed region (one copy each way per step); the copies
+          of neighbouring steps overlap the computation (two buffer sets, their own streams);
+          e2e.serial is the same without the overlap.
 roofline: the product kernel.  Average launch duration = the timed region's device time
           over its product launches (fused path: every launch of the step); otherwise a graph
           of the product calls alone, replayed like the timed region.  Algorithmic bytes (or
@@ -417,6 +419,19 @@ class DecodeStack:
         self._fused_ok = {}
         torch.cuda.synchronize()
 
+    def bind(self, x_all, y_all):
+        """Point every GEMV's activation and output views at other flat buffers of the same
+        sizes (the pipelined end-to-end loop alternates two sets)."""
+        oi = oo = 0
+        for d in self.L:
+            for name, N, K, pro in self.plan:
+                e = d[name]
+                e["x"] = x_all[oi:oi + self.M * K].view(self.M, K)
+                oi += self.M * K
+                e["y"] = y_all[oo:oo + self.M * N].view(self.M, N)
+                oo += self.M * N
+        self.x_all, self.y_all = x_all, y_all
+
     def launches_per_step(self, fused=True):
         """Kernel launches of one step: 1 per GEMV when fused; otherwise the quantisation
         plus the GEMV (M <= 16) or plus the activation widening and the GEMM (M > 16)."""
@@ -632,11 +647,17 @@ def measure(tw, workload: str, steps: int, warmup: int, world: int, separate: bo
     else:
         kern = "tw::gemm::gemm_tok_kernel / gemm_tma_kernel (tcgen05)"
 
-    # ---- e2e: inputs from pinned host, outputs back to pinned host, per step (one copy each way)
+    # ---- e2e: every step's inputs from pinned host memory and its outputs back to pinned host
+    # memory inside the timed region (one copy each way per step).  Serial: copy in, step,
+    # copy out, one after another.  Pipelined (the reported e2e): two sets of device buffers
+    # and two graphs; the upload of step t + 1 and the download of step t - 1 run on their own
+    # streams while step t computes, ordered by events (a buffer is refilled only after the
+    # step that read it, and overwritten only after its outputs were downloaded).
     h_in = stack.x_all.cpu().pin_memory()
     h_out = torch.empty(stack.y_all.shape, dtype=torch.float32).pin_memory()
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_out.numel() * h_out.element_size()
+    n_e2e = max(1, min(steps, e2e_steps))
 
     def e2e_step():
         stack.x_all.copy_(h_in, non_blocking=True)
@@ -646,7 +667,6 @@ def measure(tw, workload: str, steps: int, warmup: int, world: int, separate: bo
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    n_e2e = max(1, min(steps, e2e_steps))
     barrier(world)
     e0, e1 = events_new(), events_new()
     e0.record()
@@ -654,7 +674,58 @@ def measure(tw, workload: str, steps: int, warmup: int, world: int, separate: bo
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_el, e2e_bytes = combine_over_ranks(e0.elapsed_time(e1) / 1e3, bytes_per_step * n_e2e, world)
+    serial_el, serial_bytes = combine_over_ranks(e0.elapsed_time(e1) / 1e3, bytes_per_step * n_e2e, world)
+
+    xs_ = [stack.x_all, torch.empty_like(stack.x_all)]
+    ys_ = [stack.y_all, torch.empty_like(stack.y_all)]
+    stack.bind(xs_[1], ys_[1])
+    graph_b = capture(stack, fused)
+    stack.bind(xs_[0], ys_[0])
+    graphs = [graph, graph_b]
+    h_ins = [h_in, h_in.clone().pin_memory()]
+    h_outs = [h_out, torch.empty_like(h_out).pin_memory()]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def pipelined(n):
+        ev = lambda: torch.cuda.Event()
+        ev_in, ev_comp, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        start, stop = events_new(), events_new()
+        start.record(comp)
+        s_in.wait_event(start)
+        with torch.cuda.stream(s_in):
+            xs_[0].copy_(h_ins[0], non_blocking=True)
+            ev_in[0].record(s_in)
+        for t in range(n):
+            b = t % 2
+            comp.wait_event(ev_in[b])
+            if t >= 2:
+                comp.wait_event(ev_out[b])  # the outputs of step t - 2 have been downloaded
+            graphs[b].replay()
+            ev_comp[b].record(comp)
+            if t + 1 < n:
+                nb = 1 - b
+                with torch.cuda.stream(s_in):
+                    if t >= 1:
+                        s_in.wait_event(ev_comp[nb])  # step t - 1 has read its inputs
+                    xs_[nb].copy_(h_ins[nb], non_blocking=True)
+                    ev_in[nb].record(s_in)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[b])
+                h_outs[b].copy_(ys_[b], non_blocking=True)
+                ev_out[b].record(s_out)
+        comp.wait_event(ev_out[0])
+        comp.wait_event(ev_out[1])
+        stop.record(comp)
+        return start, stop
+
+    pipelined(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    p0, p1 = pipelined(n_e2e)
+    torch.cuda.synchronize()
+    e2e_el, e2e_bytes = combine_over_ranks(p0.elapsed_time(p1) / 1e3, bytes_per_step * n_e2e, world)
+    del graph_b
 
     res = {"value": value, "unit": UNIT, "ms_per_step": ms_per_step,
            "us_per_layer": ms_per_step * 1e3 / layers, "M": M, "layers": layers,
@@ -670,7 +741,11 @@ def measure(tw, workload: str, steps: int, warmup: int, world: int, separate: bo
                                    + "; launches overlap under programmatic dependent launch, so this is "
                                      "step time / launches, not one kernel's duration")},
            "e2e": {"value": e2e_bytes / e2e_el / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h},
+                   "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                   "how": "pipelined: two buffer sets, uploads and downloads on their own streams overlap "
+                          "the neighbouring steps' computation; every step's inputs and outputs cross",
+                   "serial": {"value": serial_bytes / serial_el / 1e9, "unit": UNIT,
+                              "how": "copy in, step, copy out, one after another"}},
            "wall_s_timed": t_wall, "elapsed_s": elapsed_max}
     return res, stack, graph, fused
 

@@ -334,6 +334,30 @@ def test_quant_gemv_parity(tw, M, N, K, rms):
     assert tw.tw_device_status() == 0
 
 
+@pytest.mark.parametrize("N,K,rms", [(30000, 2560, True), (30000, 2560, False), (8000, 8192, True),
+                                     (9001, 8192, False), (2500, 14336, False), (30000, 4096, True)])
+def test_quant_gemv_one_token_large_blocks(tw, N, K, rms):
+    """One token, quantisation fused, on matrices whose CTA block exceeds the one-token
+    kernel's shared memory (the streaming kernel takes them): K = 2560 to 14336, with and
+    without RMSNorm, row counts that do not divide evenly over the CTAs.  Every output against
+    the oracle."""
+    W, x = si.gemv_case(1, N, K, seed=N + K, outliers=True)
+    g = si.rms_gain(K, seed=K + 1) if rms else None
+    p_ref, g_ref = oracle.pack_ternary(W)
+    if rms:
+        q_ref, s_ref, sum_ref = oracle.rmsnorm_quant_act(x, g, si.RMS_EPS)
+    else:
+        q_ref, s_ref, sum_ref = oracle.quant_act(x)
+    y_ref, acc_ref = oracle.ternary_matmul(p_ref, g_ref, q_ref, s_ref, openmp=True)
+    y, acc, xq, sx, xs, y2 = fused_run(tw, x, p_ref, g_ref, g)
+    assert (xq == q_ref).all() and (xs == sum_ref).all()
+    assert (sx.view(np.uint32) == s_ref.view(np.uint32)).all()
+    assert (acc == acc_ref).all()
+    assert_y_close(y, y_ref)
+    assert (y2 == y).all()
+    assert tw.tw_device_status() == 0
+
+
 def test_quant_gemv_special_rows(tw):
     K, N = 64, 40
     x = special_rows(K)
