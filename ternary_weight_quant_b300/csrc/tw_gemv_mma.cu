@@ -162,12 +162,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
     if (STAGE == 2 && blockIdx.x + gridDim.x < nblk_all) issue(blockIdx.x + gridDim.x, 1);
   }
   const float gam = __ldg(a.w_scale);
+  if (tid < MP) xsum_s[tid] = 0;
+  __syncthreads();  // the mbarriers' initialisation and the zeroed sums, before the wait
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid < MP) {
-    xsum_s[tid] = 0;
-    cs_s[tid] = tid < a.M ? dequant_scale(gam, a.s_x[tid]) : 0.0f;
-  }
-  __syncthreads();
+  // the dequantisation scales are read only by the epilogue, behind the barrier that ends
+  // the products: their loads need not hold anything up here
+  if (tid < MP) cs_s[tid] = tid < a.M ? dequant_scale(gam, a.s_x[tid]) : 0.0f;
 
   // per-lane constants of the A masks and B scales (see the header)
   const uint32_t sh = q == 3 ? 12u : 0u;
