@@ -232,7 +232,27 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&wbar[buf]), STAGE == 2 ? (uint32_t)((b >> 1) & 1) : 0u));
       if (!ok && lane == 0) atomicCAS(&g_mma_status, 0, (int)TW_ERR_TIMEOUT);
     }
-    if (ok && g0 < g1) load_w(g0);
+    // the activation words of a group (four 16-steps) for this lane's quad position (plain
+    // loads: x_q was written by the previous kernel, read after the dependency wait); with 8
+    // tokens they are requested one group ahead, like the weight words (16 tokens: registers)
+    constexpr bool kXAhead = NT == 1;
+    uint32_t xlo_n[4][NT], xhi_n[4][NT];
+    auto load_x = [&](int gi) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const uint32_t* xp = X + ((size_t)min(n * 8 + rq, a.M - 1) * K >> 2) + 16 * gi;
+        const bool in = n * 8 + rq < a.M;
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          xlo_n[s4][n] = in ? xp[4 * s4 + xw_lo] : 0u;
+          xhi_n[s4][n] = in ? xp[4 * s4 + xw_lo + 2] : 0u;
+        }
+      }
+    };
+    if (ok && g0 < g1) {
+      load_w(g0);
+      if (kXAhead) load_x(g0);
+    }
     for (int gi = ok ? g0 : g1; gi < g1; ++gi) {
       uint4 ca[TWM], cb[TWM];
 #pragma unroll
@@ -240,10 +260,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
         ca[i] = wa[i];
         cb[i] = wb[i];
       }
-      if (gi + 1 < g1) load_w(gi + 1);  // the next group's words are in flight during this one
+      if (!kXAhead) load_x(gi);
+      uint32_t xlo[4][NT], xhi[4][NT];
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          xlo[s4][n] = xlo_n[s4][n];
+          xhi[s4][n] = xhi_n[s4][n];
+        }
+      if (gi + 1 < g1) {  // the next group's words are in flight during this one
+        load_w(gi + 1);
+        if (kXAhead) load_x(gi + 1);
+      }
       // B for token n * 8 + rq: this lane's four activations x[o0], x[o0 + 8], x[o1], x[o1 + 8]
-      // of a 16-step, scaled and in f16 (tokens past M: x = 0).  Plain loads: x_q was written by
-      // the previous kernel (read after the dependency wait).  Sums of x_q: first block only.
+      // of a 16-step, scaled and in f16 (tokens past M: x = 0).  Sums of x_q: first block only.
       auto make_b = [&](uint32_t lo, uint32_t hi, int n, uint32_t& b0, uint32_t& b1) {
         const uint32_t xb = __byte_perm(lo, hi, xsel);
         if (b == 0 && n * 8 + rq < a.M) xs_lane[n] = __dp4a((int)xb, 0x01010101, xs_lane[n]);
@@ -251,18 +282,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
         b0 = hfma2_bits(__byte_perm(u, 0x6464u, 0x4140u), sc0, nb0);
         b1 = hfma2_bits(__byte_perm(u, 0x6464u, 0x4342u), sc1, nb1);
       };
-      // the group's activation words all at once, then four 16-steps
-      uint32_t xlo[4][NT], xhi[4][NT];
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const uint32_t* xp = X + ((size_t)min(n * 8 + rq, a.M - 1) * K >> 2) + 16 * gi;
-        const bool in = n * 8 + rq < a.M;
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          xlo[s4][n] = in ? xp[4 * s4 + xw_lo] : 0u;
-          xhi[s4][n] = in ? xp[4 * s4 + xw_lo + 2] : 0u;
-        }
-      }
 #pragma unroll
       for (int s4 = 0; s4 < 4; ++s4) {
         uint32_t b0[NT], b1[NT];
