@@ -31,6 +31,8 @@
 #include "tw_common.cuh"
 
 #include <algorithm>
+#include <mutex>
+#include <vector>
 
 namespace tw {
 
@@ -465,7 +467,285 @@ __device__ __forceinline__ void fused_prologue(const StreamArgs& a, uint4* xs, f
   }
 }
 
-template <int MT, int JMAX, int PRE, bool FUSED, bool RMS>
+// ---------------------------------------------------------------------------
+// Fused prologue shared by a thread-block cluster.  Every CTA needs all of x_q, and with
+// the whole row quantised in each of up to 296 CTAs a long row costs several us after the
+// dependency wait, while the weight stream stands (each CTA reads the fp32 row from L2 two
+// or three times and spends some 30 instructions per element on it: 10 us of a 26 us
+// launch at K = 28672).  With C CTAs in a cluster, CTA rank r handles only the
+// 16-element groups [r gw, (r + 1) gw) (gw = ceil(K / 16 / C)) and the ranks exchange
+// through distributed shared memory, always by pushing into the peers' own slots so
+// that no CTA reads another's shared memory:
+//   (0) an arrive at kernel start, waited for before the first remote store (every CTA
+//       of the cluster has then started);
+//   (1) per token the largest |x| and, with RMSNorm, the float-float sum of squares of
+//       the chunk, pushed to every rank; each rank combines the C values in rank order,
+//       so every CTA of the cluster takes the same mean-square decision (the exact path,
+//       when taken, runs over the whole row in every CTA);
+//   (2) with RMSNorm, the largest |u| of the chunk the same way;
+//   (3) the quantised groups, byte-transposed, stored into the xs of every rank, and the
+//       chunk's sum of x_q into rank 0.
+// The float-float sum has at most ceil(K / 4 / C / threads) steps per accumulator, two
+// levels per thread, five per warp, a sequence of 12 over the warps and one of C over
+// the ranks: well inside the error bound that the mean-square decision assumes, so a
+// decided mean square is the exact one, as in one CTA.  x_q, s_x and x_sum are written by
+// cluster 0.
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cl_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+constexpr int kMaxCluster = 4;  // clusters of 2 or 4 CTAs
+
+template <typename T>
+__device__ __forceinline__ T* peer(T* p, uint32_t rank) {
+  return static_cast<T*>(__cluster_map_shared_rank(static_cast<void*>(p), rank));
+}
+
+template <int MT>
+struct ClusterSlots {
+  uint32_t mx[kMaxCluster][MT];  // [source rank][token] largest |x| bits of the chunk
+  float2 ff[kMaxCluster][MT];    // float-float sum of squares of the chunk
+  uint32_t am[kMaxCluster][MT];  // largest |u| bits of the chunk
+  int qs[kMaxCluster][MT];       // sum of x_q over the chunk (rank 0's copy is read)
+};
+
+template <int MT, bool RMS>
+__device__ __forceinline__ void cluster_prologue(const StreamArgs& a, uint4* xs, float* s_scale, ClusterSlots<MT>& cs,
+                                                 uint32_t* red_u, uint32_t* red_a, float2* red_ff, int* red_i,
+                                                 unsigned long long* red_lo, unsigned long long* red_hi,
+                                                 uint32_t (*limb)[256], unsigned long long* hist, double* s_dbl,
+                                                 float* s_inv, int* s_slow) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = a.K, Kw = K >> 4, K4 = K >> 2;
+  const uint32_t rank = cl_rank(), C = cl_size();
+  const bool first = blockIdx.x < C;  // cluster 0 writes the optional outputs
+  const int gw = (Kw + (int)C - 1) / (int)C;
+  const int u0 = 4 * min(Kw, (int)rank * gw), u1 = 4 * min(Kw, ((int)rank + 1) * gw);  // float4 range
+  const float4* g4 = reinterpret_cast<const float4*>(a.g);
+  // padding tokens: zeros in this CTA's own xs (no rank writes them)
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+    if (m >= a.M)
+      for (int i = tid; i < Kw; i += kThreads) xs[m * Kw + i] = make_uint4(0u, 0u, 0u, 0u);
+
+  // (1) chunk statistics
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    uint32_t mx = 0u;
+    FF s0 = {0.0f, 0.0f}, s1 = {0.0f, 0.0f}, s2 = {0.0f, 0.0f}, s3 = {0.0f, 0.0f};
+    if (m < a.M) {
+      const float4* xg = reinterpret_cast<const float4*>(a.x + (size_t)m * K);
+      for (int u = u0 + tid; u < u1; u += kThreads) {
+        const float4 v = xg[u];
+        mx = max(mx, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                         max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+        if (RMS) {
+          ff_add_square(s0, v.x);
+          ff_add_square(s1, v.y);
+          ff_add_square(s2, v.z);
+          ff_add_square(s3, v.w);
+        }
+      }
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (RMS) {
+      ff_add(s0, s1);
+      ff_add(s2, s3);
+      ff_add(s0, s2);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        FF t;
+        t.hi = __shfl_xor_sync(0xffffffffu, s0.hi, o);
+        t.lo = __shfl_xor_sync(0xffffffffu, s0.lo, o);
+        ff_add(s0, t);
+      }
+    }
+    if (lane == 0) {
+      red_u[warp * MT + m] = mx;
+      if (RMS) red_ff[warp * MT + m] = make_float2(s0.hi, s0.lo);
+    }
+  }
+  __syncthreads();
+  cl_wait();  // (0): every CTA of the cluster runs; remote stores are allowed from here
+  if (tid < (int)C * MT) {  // the CTA's totals (fixed order) to rank tid / MT
+    const int m = tid % MT;
+    uint32_t mx = 0u;
+    FF t = {0.0f, 0.0f};
+    for (int w = 0; w < kWarps; ++w) {
+      mx = max(mx, red_u[w * MT + m]);
+      if (RMS) {
+        const float2 f = red_ff[w * MT + m];
+        ff_add(t, FF{f.x, f.y});
+      }
+    }
+    const uint32_t dst = (uint32_t)(tid / MT);
+    *peer(&cs.mx[rank][m], dst) = mx;
+    if (RMS) *peer(&cs.ff[rank][m], dst) = make_float2(t.hi, t.lo);
+  }
+  cl_arrive();
+  cl_wait();  // (1)
+  uint32_t am[MT];
+  float inv[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    am[m] = 0u;
+    inv[m] = 1.0f;
+  }
+  if constexpr (RMS) {
+    bool okm[MT];
+    bool slow = false;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      FF t = {0.0f, 0.0f};
+      for (uint32_t r = 0; r < C; ++r) {
+        const float2 f = cs.ff[r][m];
+        ff_add(t, FF{f.x, f.y});
+      }
+      float ms = 0.0f;
+      okm[m] = m >= a.M || ff_mean_f32(t, K, a.inv_k, ms);
+      inv[m] = okm[m] ? inv_rms_f32(ms, a.eps) : 0.0f;
+      slow |= !okm[m];
+    }
+    if (slow) {  // cluster-uniform: every CTA combined the same values in the same order
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+        if (!okm[m])
+          inv[m] = rms_inv_exact<kWarps>(reinterpret_cast<const float4*>(a.x + (size_t)m * K), K4, a.kd, a.eps,
+                                         red_u + kWarps * MT, red_lo, red_hi, limb, hist, s_dbl, s_inv, s_slow);
+    }
+    // (2) largest |u| of the chunk, u = fl(fl(x inv) g)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      uint32_t t = 0u;
+      if (m < a.M) {
+        const float4* xg = reinterpret_cast<const float4*>(a.x + (size_t)m * K);
+        for (int u = u0 + tid; u < u1; u += kThreads) {
+          const float4 v = xg[u];
+          const float4 gg = g4[u];
+          const float4 w = make_float4(__fmul_rn(__fmul_rn(v.x, inv[m]), gg.x), __fmul_rn(__fmul_rn(v.y, inv[m]), gg.y),
+                                       __fmul_rn(__fmul_rn(v.z, inv[m]), gg.z), __fmul_rn(__fmul_rn(v.w, inv[m]), gg.w));
+          t = max(t, __float_as_uint(fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w)))));
+        }
+      }
+      t = __reduce_max_sync(0xffffffffu, t);
+      if (lane == 0) red_a[warp * MT + m] = t;
+    }
+    __syncthreads();
+    if (tid < (int)C * MT) {
+      const int m = tid % MT;
+      uint32_t t = 0u;
+      for (int w = 0; w < kWarps; ++w) t = max(t, red_a[w * MT + m]);
+      *peer(&cs.am[rank][m], (uint32_t)(tid / MT)) = t;
+    }
+    cl_arrive();
+    cl_wait();  // (2)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      for (uint32_t r = 0; r < C; ++r) am[m] = max(am[m], cs.am[r][m]);
+  } else {
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      for (uint32_t r = 0; r < C; ++r) am[m] = max(am[m], cs.mx[r][m]);
+  }
+
+  // (3) quantise the chunk: lane l takes float4 u = base + l (base a multiple of 32, so the
+  // four float4s of a group sit in lanes 4q..4q+3 and the chunk ends on a group boundary)
+  int qsum[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    qsum[m] = 0;
+    if (m >= a.M) continue;
+    const float amax = __uint_as_float(am[m]);
+    // the conversion-free rounding of the single-CTA quantisation, with the same checks
+    float ra = amax == 0.0f ? 0.0f : __int_as_float(0x7fffffff);
+    if (amax >= 0x1p-120f && amax <= 0x1p120f) asm("rcp.approx.f32 %0, %1;" : "=f"(ra) : "f"(amax));
+    const float4* xg = reinterpret_cast<const float4*>(a.x + (size_t)m * K);
+    uint32_t* qout = a.x_q_out ? reinterpret_cast<uint32_t*>(a.x_q_out + (size_t)m * K) : nullptr;
+    for (int base = u0 + warp * 32; base < u1; base += kThreads) {  // warp-uniform trip count
+      const int u = base + lane;
+      const bool act = u < u1;
+      float e[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      uint32_t pq = 0u;
+      bool near = false;
+      if (act) {
+        const float4 v = xg[u];
+        if (RMS) {
+          const float4 gg = g4[u];
+          e[0] = __fmul_rn(__fmul_rn(v.x, inv[m]), gg.x);
+          e[1] = __fmul_rn(__fmul_rn(v.y, inv[m]), gg.y);
+          e[2] = __fmul_rn(__fmul_rn(v.z, inv[m]), gg.z);
+          e[3] = __fmul_rn(__fmul_rn(v.w, inv[m]), gg.w);
+        } else {
+          e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float d = __fmul_rn(__fmul_rn(e[j], 127.0f), ra);
+          const float sb = __fadd_rn(d, 12582912.0f);  // d + 1.5 2^23: rounds d to an integer
+          near |= !(fabsf(__fsub_rn(d, __fsub_rn(sb, 12582912.0f))) < 0.49995f);  // also non-finite d
+          const int t = (int)(__float_as_uint(sb) & 0x7fffffu) - 0x400000;
+          pq |= ((uint32_t)max(-128, min(127, t)) & 0xffu) << (8 * j);
+        }
+      }
+      if (__any_sync(0xffffffffu, near) && near) {  // rare: the IEEE divide
+        pq = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int t = amax > 0.0f ? __float2int_rn(__fdiv_rn(__fmul_rn(e[j], 127.0f), amax)) : 0;
+          pq |= ((uint32_t)max(-128, min(127, t)) & 0xffu) << (8 * j);
+        }
+      }
+      const uint32_t p1 = __shfl_down_sync(0xffffffffu, pq, 1);
+      const uint32_t p2 = __shfl_down_sync(0xffffffffu, pq, 2);
+      const uint32_t p3 = __shfl_down_sync(0xffffffffu, pq, 3);
+      if (act) {
+        qsum[m] += (int)(int8_t)(pq & 0xffu) + (int)(int8_t)((pq >> 8) & 0xffu) + (int)(int8_t)((pq >> 16) & 0xffu) +
+                   (int)(int8_t)(pq >> 24);
+        if (first && qout) qout[u] = pq;
+        if ((lane & 3) == 0) {
+          const uint4 grp = permute_group(make_uint4(pq, p1, p2, p3));
+          uint4* dst = xs + m * Kw + (u >> 2);
+          for (uint32_t r = 0; r < C; ++r) *peer(dst, r) = grp;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    qsum[m] = __reduce_add_sync(0xffffffffu, qsum[m]);
+    if (lane == 0) red_i[warp * MT + m] = qsum[m];
+  }
+  __syncthreads();
+  if (tid < MT) {
+    int t = 0;
+    for (int w = 0; w < kWarps; ++w) t += red_i[w * MT + tid];
+    *peer(&cs.qs[rank][tid], 0u) = t;
+    s_scale[tid] = __uint_as_float(am[tid]);
+  }
+  cl_arrive();
+  cl_wait();  // (3): xs complete in every CTA of the cluster
+  if (blockIdx.x == 0 && tid < a.M) {
+    if (a.x_sum_out) {
+      int t = 0;
+      for (uint32_t r = 0; r < C; ++r) t += cs.qs[r][tid];
+      a.x_sum_out[tid] = t;
+    }
+    if (a.s_x_out) a.s_x_out[tid] = __uint_as_float(am[tid]);
+  }
+}
+
+// CL: launched in clusters of 2 or 4 CTAs that share the fused prologue (cluster_prologue).
+template <int MT, int JMAX, int PRE, bool FUSED, bool RMS, bool CL = false>
 __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -486,8 +766,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
   __shared__ double s_dbl;
   __shared__ uint32_t limb[RMS ? 3 : 1][256];
   __shared__ unsigned long long hist[RMS ? 256 : 1];
+  __shared__ ClusterSlots<CL ? MT : 1> cslots;
 
   pdl_launch_dependents();
+  if constexpr (CL) cl_arrive_relaxed();  // (0) of the cluster prologue
 
   // ---------------------------------------------------------------- rows of this warp
   const int S = a.S, G = kWarps / S;
@@ -544,6 +826,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
       }
     }
     if (tid < MT) s_scale[tid] = tid < a.M ? a.s_x_in[tid] : 0.0f;
+  } else if constexpr (CL) {
+    cluster_prologue<MT, RMS>(a, xs, s_scale, cslots, red_u, red_a, red_ff, red_i, red_lo, red_hi, limb, hist,
+                              &s_dbl, s_inv, s_slow);
   } else {
     float* xf = a.xf_off >= 0 ? reinterpret_cast<float*>(smem + a.xf_off) : nullptr;
     fused_prologue<MT, RMS>(a, xs, xf, s_scale, red_u, red_a, red_ff, red_i, red_lo, red_hi, limb, hist, &s_dbl,
@@ -1159,10 +1444,16 @@ struct Plan {
   int grid, rows_base, rows_rem, S, jmax;
   int xs_off, acc_off, xf_off;
   int h_off = 0;
+  int cl = 1;  // streaming kernel with the fused prologue: CTAs per cluster sharing it
   size_t smem;
 };
 
 constexpr int kMaxRowsPerCta = 8192;
+// Rows of at least this many weights share the fused quantisation across a cluster.  Below
+// it the per-CTA prologue is shorter than the cluster's extra barrier rounds (measured on the
+// 8B and 70B shapes: K = 14336 and 28672 gain 0.4 to 8 us per launch, K = 4096 and 8192 lose up
+// to 1.5 us without RMSNorm).
+constexpr int kClusterMinK = 12288;
 // Dynamic shared memory of the one-token decode kernel: at most this much, so that the
 // next launch's CTA (programmatic dependent launch) fits on the SM beside it.
 constexpr size_t kDecodeSmemMax = 110 * 1024;
@@ -1205,7 +1496,10 @@ bool make_plan(int M, int N, int K, int num_sms, Plan& p, bool fused, bool rms =
   // token (the decode kernel) may stage more, as long as two CTAs still fit on an SM
   const size_t stage = (size_t)(MT + (rms ? 1 : 0)) * K * 4;
   p.xf_off = -1;
-  if (fused && stage <= 64 * 1024) {
+  // From K = kClusterMinK the CTAs share the quantisation in clusters of 4 CTAs (the
+  // launcher falls back to 2 when too few clusters of 4 can be resident).
+  p.cl = fused && K >= kClusterMinK && p.grid >= 2 ? 4 : 1;
+  if (fused && p.cl == 1 && stage <= 64 * 1024) {
     p.xf_off = (int)p.smem;
     p.smem += stage;
   }
@@ -1215,21 +1509,104 @@ bool make_plan(int M, int N, int K, int num_sms, Plan& p, bool fused, bool rms =
 // Rows per warp loaded ahead: about 40 words of weights per lane.
 constexpr int pre_for(int MT, int J) { return MT == 1 ? (J <= 5 ? 8 : 6) : MT == 2 ? (J <= 2 ? 8 : 6) : (J <= 1 ? 8 : 4); }
 
+// Clusters of C CTAs of `kern` (with `smem` bytes of dynamic shared memory each) that can be
+// resident at once on the current device.  The occupancy query is made once per device,
+// kernel, C and shared memory.  Clusters stay within a GPC, so on a part whose GPCs do not
+// hold a multiple of C CTAs fewer than grid / C fit: on 148 SMs, 74 clusters of 2 at one or
+// two CTAs per SM, but 33 of 4 at one CTA per SM and 71 of 4 at two.
+int max_clusters(const void* kern, size_t smem, int C) {
+  struct Entry {
+    int dev;
+    const void* kern;
+    size_t smem;
+    int C, clusters;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (const Entry& e : cache)
+      if (e.dev == dev && e.kern == kern && e.smem == smem && e.C == C) return e.clusters;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C);
+  cfg.blockDim = dim3(tw::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();  // not sticky; the caller launches without clusters
+    n = 0;
+  }
+  std::lock_guard<std::mutex> g(mu);
+  cache.push_back(Entry{dev, kern, smem, C, n});
+  return n;
+}
+
 template <int MT, int JMAX, bool FUSED, bool RMS>
 cudaError_t launch(const tw::StreamArgs& a, const Plan& p, cudaStream_t stream, bool pdl) {
-  auto kern = tw::gemv_stream_kernel<MT, JMAX, pre_for(MT, JMAX), FUSED, RMS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);
   cfg.blockDim = dim3(tw::kThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
+  if constexpr (FUSED) {
+    // The largest C (from the plan's down to 2) whose resident clusters cover the grid, or at
+    // least 95 % of it (the grid then shrinks to those clusters, each CTA taking a few more
+    // rows); with none, one CTA per cluster (x then comes from global memory: xf_off is -1).
+    auto kc = tw::gemv_stream_kernel<MT, JMAX, pre_for(MT, JMAX), FUSED, RMS, true>;
+    for (int C = p.cl; C >= 2; C /= 2) {
+      const int grid = p.grid / C * C;
+      if (grid < C) continue;
+      tw::StreamArgs b = a;
+      b.rows_base = a.N / grid;
+      b.rows_rem = a.N % grid;
+      const int max_rows = b.rows_base + (b.rows_rem ? 1 : 0);
+      if (max_rows > kMaxRowsPerCta) continue;
+      const size_t smem = (size_t)p.acc_off + ((size_t)max_rows * MT * 4 + 15) / 16 * 16;
+      cudaError_t e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      const long long fit = (long long)max_clusters((const void*)kc, smem, C) * C;
+      if (20 * fit < 19LL * p.grid) continue;
+      const int g = fit < grid ? (int)fit : grid;
+      b.rows_base = a.N / g;
+      b.rows_rem = a.N % g;
+      const int rows_g = b.rows_base + (b.rows_rem ? 1 : 0);
+      const size_t smem_g = (size_t)p.acc_off + ((size_t)rows_g * MT * 4 + 15) / 16 * 16;
+      if (smem_g != smem) {
+        e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_g);
+        if (e != cudaSuccess) return e;
+      }
+      cfg.gridDim = dim3((unsigned)g);
+      cfg.dynamicSmemBytes = smem_g;
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = (unsigned)C;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      cfg.numAttrs = na + 1;
+      return cudaLaunchKernelEx(&cfg, kc, b);
+    }
+  }
+  auto kern = tw::gemv_stream_kernel<MT, JMAX, pre_for(MT, JMAX), FUSED, RMS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

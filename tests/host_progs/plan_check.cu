@@ -19,8 +19,8 @@ int main() {
         std::printf("none\n");
         continue;
       }
-      std::printf("grid %d rows_base %d rows_rem %d S %d jmax %d xs_off %d acc_off %d xf_off %d smem %zu\n", p.grid,
-                  p.rows_base, p.rows_rem, p.S, p.jmax, p.xs_off, p.acc_off, p.xf_off, p.smem);
+      std::printf("grid %d rows_base %d rows_rem %d S %d jmax %d xs_off %d acc_off %d xf_off %d cl %d smem %zu\n",
+                  p.grid, p.rows_base, p.rows_rem, p.S, p.jmax, p.xs_off, p.acc_off, p.xf_off, p.cl, p.smem);
     } else {
       GemmPlan p;
       bool ok;
