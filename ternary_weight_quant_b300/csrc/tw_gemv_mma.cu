@@ -260,7 +260,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
         ca[i] = wa[i];
         cb[i] = wb[i];
       }
-      if (!kXAhead) load_x(gi);
+      // the next group's words are in flight during this one; with 16 tokens the weight words
+      // are requested before this group's activation words
+      if (!kXAhead) {
+        if (gi + 1 < g1) load_w(gi + 1);
+        load_x(gi);
+      }
       uint32_t xlo[4][NT], xhi[4][NT];
 #pragma unroll
       for (int s4 = 0; s4 < 4; ++s4)
@@ -269,9 +274,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(Args a) {
           xlo[s4][n] = xlo_n[s4][n];
           xhi[s4][n] = xhi_n[s4][n];
         }
-      if (gi + 1 < g1) {  // the next group's words are in flight during this one
+      if (kXAhead && gi + 1 < g1) {
         load_w(gi + 1);
-        if (kXAhead) load_x(gi + 1);
+        load_x(gi + 1);
       }
       // B for token n * 8 + rq: this lane's four activations x[o0], x[o0 + 8], x[o1], x[o1 + 8]
       // of a 16-step, scaled and in f16 (tokens past M: x = 0).  Sums of x_q: first block only.
