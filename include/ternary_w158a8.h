@@ -217,7 +217,7 @@ TW_API tw_status tw_ternary_gemv(const uint8_t *packed, const float *w_scale, co
  * (weights packed at load time, with any later synchronisation or any other
  * kernel in between, are fine).  The same holds for w_scale and the RMSNorm gain
  * g, which are also read before that point.
- * From K = 12288, when more than one CTA runs (rows that the one-token kernel's shared
+ * From K = 12288 (8192 with RMSNorm), when more than one CTA runs (rows that the one-token kernel's shared
  * memory does not hold), the CTAs are launched in thread-block clusters of 4 (2 where too
  * few clusters of 4 can be resident) and each CTA quantises only its share of K, exchanging
  * the partial statistics and the quantised groups through distributed shared memory; the

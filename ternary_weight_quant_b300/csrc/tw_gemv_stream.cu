@@ -32,6 +32,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 namespace tw {
@@ -49,6 +50,25 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   int d;
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
+}
+
+// The packed word at byte offset OFF from p when bit BIT of ok is set: one predicated load,
+// its predicate formed inside, no branch.  Otherwise v is left undefined; the callers
+// multiply such words by x = 0, so any value gives the same result.
+template <int OFF, uint32_t BIT>
+__device__ __forceinline__ void ld_stream_if(uint32_t& v, const uint32_t* p, uint32_t ok, uint64_t pol) {
+  asm volatile(
+      "{\n .reg .pred q;\n .reg .b32 t;\n and.b32 t, %1, %3;\n setp.ne.b32 q, t, 0;\n"
+      " @q ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%2+%4], %5;\n}\n"
+      : "=r"(v)
+      : "r"(ok), "l"(p), "n"(BIT), "n"(OFF), "l"(pol));
+}
+// Words j = 0 .. JMAX-1 of one row: word j at 128 j bytes from p (a lane's word of each
+// 32-word step), loaded where bit j of ok is set.
+template <int... J>
+__device__ __forceinline__ void ld_row_words(uint32_t* w, const uint32_t* p, uint32_t ok, uint64_t pol,
+                                             std::integer_sequence<int, J...>) {
+  (ld_stream_if<128 * J, 1u << J>(w[J], p, ok, pol), ...);
 }
 
 struct StreamArgs {
@@ -780,17 +800,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
   const uint32_t* Wp = reinterpret_cast<const uint32_t*>(a.packed) + (size_t)row0 * Kw;
   const uint64_t pol = l2_evict_first_policy();
 
+  // Word j of a row for this lane is at ws0 + lane + 32 j: one address per row, the words at
+  // immediate offsets, each load predicated on bit j of wok (the word lies in the K slice).
+  // Words outside the slice are not loaded and meet x = 0; rows past the group's end read
+  // its first row again (their sums are never formed).
   uint32_t wv[PRE][JMAX];
+  uint32_t wok = 0u;
+#pragma unroll
+  for (int j = 0; j < JMAX; ++j)
+    if (ws0 + lane + 32 * j < ws1) wok |= 1u << j;
+  const uint32_t* Wl = Wp + (size_t)gr * Kw + ws0 + lane;
+  const size_t rstride = (size_t)G * Kw;
   auto load_batch = [&](int b) {
 #pragma unroll
     for (int p = 0; p < PRE; ++p) {
       const int i = b * PRE + p;
-      const uint32_t* rowp = Wp + (size_t)(gr + (i < nr ? i : 0) * G) * Kw;
-#pragma unroll
-      for (int j = 0; j < JMAX; ++j) {
-        const int wi = ws0 + lane + 32 * j;
-        wv[p][j] = (i < nr && wi < ws1) ? ld_stream_u32(rowp + wi, pol) : 0x55555555u;
-      }
+      ld_row_words(wv[p], Wl + (size_t)(i < nr ? i : 0) * rstride, wok, pol, std::make_integer_sequence<int, JMAX>{});
     }
   };
   // weights (and their scale) do not depend on the previous kernel: start streaming now
@@ -875,8 +900,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(StreamArgs a) 
         }
       }
       const int i = b * PRE + p;
-      // padding words hold code 1 (weight 0) against x = 0; lane_xsum covers exactly the
-      // words this lane multiplied.  acc[m][s] is 4^s times an integer: the shifts are exact.
+      // words outside the K slice meet x = 0; lane_xsum covers exactly the words this lane
+      // multiplied.  acc[m][s] is 4^s times an integer: the shifts are exact.
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
         const int t = acc[m][0] + (acc[m][1] >> 2) + (acc[m][2] >> 4) + (acc[m][3] >> 6) - lane_xsum[m];
@@ -1451,9 +1476,11 @@ struct Plan {
 constexpr int kMaxRowsPerCta = 8192;
 // Rows of at least this many weights share the fused quantisation across a cluster.  Below
 // it the per-CTA prologue is shorter than the cluster's extra barrier rounds (measured on the
-// 8B and 70B shapes: K = 14336 and 28672 gain 0.4 to 8 us per launch, K = 4096 and 8192 lose up
-// to 1.5 us without RMSNorm).
+// 8B and 70B shapes: K = 14336 and 28672 gain 0.4 to 8 us per launch; K = 4096 loses up to
+// 1.2 us, and K = 8192 up to 1.5 us without RMSNorm; with RMSNorm K = 8192 gains up to 0.7 us
+// and its single-CTA prologue would spill registers).
 constexpr int kClusterMinK = 12288;
+constexpr int kClusterMinKRms = 8192;
 // Dynamic shared memory of the one-token decode kernel: at most this much, so that the
 // next launch's CTA (programmatic dependent launch) fits on the SM beside it.
 constexpr size_t kDecodeSmemMax = 110 * 1024;
@@ -1496,9 +1523,10 @@ bool make_plan(int M, int N, int K, int num_sms, Plan& p, bool fused, bool rms =
   // token (the decode kernel) may stage more, as long as two CTAs still fit on an SM
   const size_t stage = (size_t)(MT + (rms ? 1 : 0)) * K * 4;
   p.xf_off = -1;
-  // From K = kClusterMinK the CTAs share the quantisation in clusters of 4 CTAs (the
-  // launcher falls back to 2 when too few clusters of 4 can be resident).
-  p.cl = fused && K >= kClusterMinK && p.grid >= 2 ? 4 : 1;
+  // From K = kClusterMinK (kClusterMinKRms with RMSNorm) the CTAs share the quantisation in
+  // clusters of 4 CTAs (the launcher falls back to 2 when too few clusters of 4 can be
+  // resident).
+  p.cl = fused && K >= (rms ? kClusterMinKRms : kClusterMinK) && p.grid >= 2 ? 4 : 1;
   if (fused && p.cl == 1 && stage <= 64 * 1024) {
     p.xf_off = (int)p.smem;
     p.smem += stage;

@@ -1,5 +1,5 @@
 """GPU parity of the fused quantisation + GEMV when its CTAs share the quantisation in a
-thread-block cluster (the streaming kernel from K = 12288).
+thread-block cluster (the streaming kernel from K = 12288, and from K = 8192 with RMSNorm).
 
 Each CTA of a cluster quantises one chunk of K and pushes the chunk's statistics and its
 quantised groups to the other CTAs through distributed shared memory.  The launcher takes
@@ -82,7 +82,7 @@ def check(tw, x, W, g, rows=None):
 
 # (N, K, M): 146 rows at K = 12288 (grid 146 -> 144), 3000 (296 -> 284), 28672 with 2500 rows
 # (296 -> 284) and 1000 (148), 16448 (257 groups per rank), 2 tokens (148), 3 tokens (296 ->
-# 284), 4 tokens (148), 37 rows (grid 36), and K = 8192 below the threshold for contrast
+# 284), 4 tokens (148), 37 rows (grid 36), and K = 8192 (clusters with RMSNorm only)
 CASES = [(146, 12288, 1), (3000, 12288, 1), (2500, 28672, 1), (1000, 28672, 1), (2000, 16448, 1),
          (1000, 12288, 2), (700, 12288, 3), (300, 12288, 4), (37, 12288, 1), (640, 8192, 4)]
 
