@@ -358,6 +358,35 @@ def test_quant_gemv_one_token_large_blocks(tw, N, K, rms):
     assert tw.tw_device_status() == 0
 
 
+@pytest.mark.parametrize("N,K", [(9500, 6144), (6500, 8192), (5000, 12288), (3500, 16384)])
+def test_stream_one_token_several_batches(tw, N, K):
+    """One token on the streaming kernel with six words per lane and row and several batches
+    of rows per warp group (two CTAs per SM; with RMSNorm at K >= 8192 in clusters).  The
+    product on a given x_q and the fused launch with and without RMSNorm, every output
+    against the oracle (the 70B gate|up takes this path in tests/test_fullsize_gpu.py)."""
+    W, x = si.gemv_case(1, N, K, seed=N + 3 * K, outliers=True)
+    p_ref, g_ref = oracle.pack_ternary(W)
+    rows = np.arange(N)
+    packed, gamma = dev(p_ref), dev(np.array([g_ref], np.float32))
+    q_ref, s_ref, sum_ref = oracle.quant_act(x)
+    y_ref, acc_ref = oracle.ternary_matmul(p_ref[rows], g_ref, q_ref, s_ref, openmp=True)
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    acc = torch.empty((1, N), dtype=torch.int32, device="cuda")
+    tw.tw_ternary_gemv(packed, gamma, dev(q_ref), dev(s_ref), y, dev(sum_ref), acc)
+    assert (host(acc)[:, rows] == acc_ref).all()
+    assert_y_close(host(y)[:, rows], y_ref)
+    for g in (None, si.rms_gain(K, seed=K + 9)):
+        if g is not None:
+            q_ref, s_ref, _ = oracle.rmsnorm_quant_act(x, g, si.RMS_EPS)
+            y_ref, acc_ref = oracle.ternary_matmul(p_ref[rows], g_ref, q_ref, s_ref, openmp=True)
+        yf, accf, xq, sx, _, y2 = fused_run(tw, x, p_ref, g_ref, g)
+        assert (xq == q_ref).all() and (sx.view(np.uint32) == s_ref.view(np.uint32)).all()
+        assert (accf[:, rows] == acc_ref).all()
+        assert_y_close(yf[:, rows], y_ref)
+        assert (y2 == yf).all()
+    assert tw.tw_device_status() == 0
+
+
 def test_quant_gemv_special_rows(tw):
     K, N = 64, 40
     x = special_rows(K)
