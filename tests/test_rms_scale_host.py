@@ -157,8 +157,8 @@ def exact_ms_bits(x):
         return int(np.float32(R / len(x)).view(np.uint32))
 
 
-def run_fast(prog, rows):
-    text = "".join(f"{len(r)} " + " ".join(str(int(b)) for b in np.asarray(r, np.float32).view(np.uint32)) + "\n"
+def run_fast(prog, rows, C=0):
+    text = "".join(f"{len(r)} {C} " + " ".join(str(int(b)) for b in np.asarray(r, np.float32).view(np.uint32)) + "\n"
                    for r in rows)
     out = subprocess.run([prog], input=text, capture_output=True, text=True, check=True).stdout.split("\n")
     return [tuple(int(v) for v in line.split()) for line in out if line.strip()]
@@ -207,3 +207,28 @@ def test_fast_path_refuses_out_of_range_sums(fast_prog):
     rows = [np.full(256, 1e-30, np.float32), np.full(256, 1e25, np.float32), np.zeros(256, np.float32)]
     got = run_fast(fast_prog, rows)
     assert [ok for ok, _ in got] == [0, 0, 0]
+
+
+@pytest.mark.parametrize("C", [2, 4, 8])
+def test_fast_path_in_cluster_order(fast_prog, C):
+    """The order of the cluster-shared prologue (each rank a chunk of 16-element groups, four
+    component accumulators per thread, warp butterflies, then sequential sums over warps and
+    ranks): whenever the decision is taken, its mean square is the exact one."""
+    rng = np.random.default_rng(100 + C)
+    rows = []
+    for K in (8192, 12288, 16448, 28672):
+        for s in (1e-3, 1.0, 37.0):
+            rows.append((rng.standard_normal(K) * s).astype(np.float32))
+            rows.append(near_midpoint_row(rng, K, s, big=False))
+            rows.append(near_midpoint_row(rng, K, s, big=True))
+    for _ in range(6):
+        K = int(rng.choice([8192, 14336]))
+        rows.append((rng.standard_normal(K) * np.exp2(rng.integers(-20, 20, K))).astype(np.float32))
+    got = run_fast(fast_prog, rows, C)
+    assert len(got) == len(rows)
+    n_ok = 0
+    for x, (ok, bits) in zip(rows, got):
+        if ok:
+            n_ok += 1
+            assert bits == exact_ms_bits(x), (len(x), C, hex(bits), hex(exact_ms_bits(x)))
+    assert n_ok >= len(rows) // 2
