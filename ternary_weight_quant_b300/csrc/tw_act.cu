@@ -258,6 +258,196 @@ __global__ void __launch_bounds__(512) act_quant_kernel(const float* __restrict_
   }
 }
 
+// ---------------------------------------------------------------------------
+// The same quantisation with each token shared by a thread-block cluster of C CTAs (grid C x M,
+// clusters along x): rank r takes the float4 units [r gw, (r + 1) gw) of its token, gw =
+// ceil(K / 4 / C), so that a long row is read and quantised by C CTAs instead of one.  Each
+// rank pushes its chunk's largest |x| (with RMSNorm also its float-float sum of squares, and
+// later its largest |u|) into every peer's shared memory between cluster barriers; every rank
+// combines the C values in rank order, so all take the same decisions (the exact mean-square
+// path, when taken, runs over the whole row in every CTA of the cluster).  The chunk's x_q go
+// to global memory and its sum of x_q to rank 0, which writes s_x and x_sum.  The results are
+// those of one CTA per token: the maximum does not depend on the order, and a decided
+// float-float mean square is the exact one whatever the summation order.
+constexpr int kActClusterMax = 8;
+constexpr int kActClusterThreads = 256;
+
+template <bool RMS>
+__global__ void __launch_bounds__(kActClusterThreads) act_quant_cluster_kernel(
+    const float* __restrict__ x, const float* __restrict__ g, float eps, int K, KDiv kd, float inv_k,
+    int8_t* __restrict__ x_q, float* __restrict__ s_x, int32_t* __restrict__ x_sum) {
+  constexpr int kNW = kActClusterThreads / 32;
+  const int m = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K4 = K >> 2;
+  const uint32_t rank = cl_rank(), C = cl_size();
+  const int gw = (K4 + (int)C - 1) / (int)C;
+  const int u0 = min(K4, (int)rank * gw), u1 = min(K4, u0 + gw);
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)m * K);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  __shared__ uint32_t c_mx[kActClusterMax], c_am[kActClusterMax];  // [source rank]
+  __shared__ float2 c_ff[kActClusterMax];
+  __shared__ int c_qs[kActClusterMax];
+  __shared__ uint32_t red_u[kNW], red_a[kNW];
+  __shared__ float2 red_ff[kNW];
+  __shared__ int red_i[kNW];
+  __shared__ uint32_t limb[RMS ? 3 : 1][RMS ? 256 : 1];
+  __shared__ unsigned long long hist[RMS ? 256 : 1];
+  __shared__ unsigned long long red_lo[32], red_hi[32];
+  __shared__ float sh_inv;
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  cl_arrive_relaxed();  // (0), waited for before the first remote store
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+
+  // (1) the chunk's largest |x| and (RMSNorm) float-float sum of squares, one accumulator per
+  // vector component
+  uint32_t mx = 0u;
+  FF s0 = {0.0f, 0.0f}, s1 = {0.0f, 0.0f}, s2 = {0.0f, 0.0f}, s3 = {0.0f, 0.0f};
+  for (int u = u0 + tid; u < u1; u += kActClusterThreads) {
+    const float4 v = xr[u];
+    mx = max(mx, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                     max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+    if (RMS) {
+      ff_add_square(s0, v.x);
+      ff_add_square(s1, v.y);
+      ff_add_square(s2, v.z);
+      ff_add_square(s3, v.w);
+    }
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (RMS) {
+    ff_add(s0, s1);
+    ff_add(s2, s3);
+    ff_add(s0, s2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      FF t;
+      t.hi = __shfl_xor_sync(0xffffffffu, s0.hi, o);
+      t.lo = __shfl_xor_sync(0xffffffffu, s0.lo, o);
+      ff_add(s0, t);
+    }
+  }
+  if (lane == 0) {
+    red_u[warp] = mx;
+    if (RMS) red_ff[warp] = make_float2(s0.hi, s0.lo);
+  }
+  __syncthreads();
+  cl_wait();  // (0): every CTA of the cluster runs
+  if (tid < (int)C) {  // the CTA's totals, warps in order, to rank tid
+    uint32_t bm = 0u;
+    FF t = {0.0f, 0.0f};
+    for (int w = 0; w < kNW; ++w) {
+      bm = max(bm, red_u[w]);
+      if (RMS) ff_add(t, FF{red_ff[w].x, red_ff[w].y});
+    }
+    *peer(&c_mx[rank], (uint32_t)tid) = bm;
+    if (RMS) *peer(&c_ff[rank], (uint32_t)tid) = make_float2(t.hi, t.lo);
+  }
+  cl_arrive();
+  cl_wait();  // (1)
+  mx = 0u;
+  FF tot = {0.0f, 0.0f};
+  for (uint32_t r = 0; r < C; ++r) {
+    mx = max(mx, c_mx[r]);
+    if (RMS) ff_add(tot, FF{c_ff[r].x, c_ff[r].y});
+  }
+
+  float inv = 1.0f;
+  uint32_t am = mx;  // without RMSNorm a = max |x|
+  if constexpr (RMS) {
+    float ms = 0.0f;
+    if (ff_mean_f32(tot, K, inv_k, ms)) {
+      inv = inv_rms_f32(ms, eps);
+    } else {  // cluster-uniform
+      inv = act_rms_inv_exact(xr, K4, mx, kd, eps, limb, hist, red_lo, red_hi, &sh_inv);
+    }
+    // (2) the chunk's largest |u|
+    uint32_t t = 0u;
+    for (int u = u0 + tid; u < u1; u += kActClusterThreads) {
+      const float4 v = xr[u];
+      const float4 gg = g4[u];
+      const float4 w = make_float4(__fmul_rn(__fmul_rn(v.x, inv), gg.x), __fmul_rn(__fmul_rn(v.y, inv), gg.y),
+                                   __fmul_rn(__fmul_rn(v.z, inv), gg.z), __fmul_rn(__fmul_rn(v.w, inv), gg.w));
+      t = max(t, __float_as_uint(fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w)))));
+    }
+    t = __reduce_max_sync(0xffffffffu, t);
+    if (lane == 0) red_a[warp] = t;
+    __syncthreads();
+    if (tid < (int)C) {
+      uint32_t bm = 0u;
+      for (int w = 0; w < kNW; ++w) bm = max(bm, red_a[w]);
+      *peer(&c_am[rank], (uint32_t)tid) = bm;
+    }
+    cl_arrive();
+    cl_wait();  // (2)
+    am = 0u;
+    for (uint32_t r = 0; r < C; ++r) am = max(am, c_am[r]);
+  }
+
+  // (3) quantise the chunk: the conversion-free rounding of act_quant_kernel, with the same
+  // IEEE-divide redo near a half-integer or for a non-finite quotient
+  const float a = __uint_as_float(am);
+  float ra = a == 0.0f ? 0.0f : __int_as_float(0x7fffffff);
+  if (a >= 0x1p-120f && a <= 0x1p120f) asm("rcp.approx.f32 %0, %1;" : "=f"(ra) : "f"(a));
+  int sum = 0;
+  uint32_t* out = reinterpret_cast<uint32_t*>(x_q + (size_t)m * K);
+  for (int base = u0 + warp * 32; base < u1; base += kActClusterThreads) {  // warp-uniform trip count
+    const int i = base + lane;
+    float uu[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t pq = 0u;
+    bool near = false;
+    if (i < u1) {
+      const float4 v = xr[i];
+      float4 gg = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (RMS) gg = g4[i];
+      uu[0] = RMS ? __fmul_rn(__fmul_rn(v.x, inv), gg.x) : v.x;
+      uu[1] = RMS ? __fmul_rn(__fmul_rn(v.y, inv), gg.y) : v.y;
+      uu[2] = RMS ? __fmul_rn(__fmul_rn(v.z, inv), gg.z) : v.z;
+      uu[3] = RMS ? __fmul_rn(__fmul_rn(v.w, inv), gg.w) : v.w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float d = __fmul_rn(__fmul_rn(uu[j], 127.0f), ra);
+        const float sb = __fadd_rn(d, 12582912.0f);  // d + 1.5 2^23: rounds d to an integer
+        near |= !(fabsf(__fsub_rn(d, __fsub_rn(sb, 12582912.0f))) < 0.49995f);
+        const int q = (int)(__float_as_uint(sb) & 0x7fffffu) - 0x400000;
+        pq |= ((uint32_t)max(-128, min(127, q)) & 0xffu) << (8 * j);
+      }
+    }
+    if (__any_sync(0xffffffffu, near) && near) {  // rare
+      pq = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = a > 0.0f ? __float2int_rn(__fdiv_rn(__fmul_rn(uu[j], 127.0f), a)) : 0;
+        pq |= ((uint32_t)max(-128, min(127, q)) & 0xffu) << (8 * j);
+      }
+    }
+    if (i < u1) {
+      out[i] = pq;
+      sum += (int)(int8_t)(pq & 0xffu) + (int)(int8_t)((pq >> 8) & 0xffu) + (int)(int8_t)((pq >> 16) & 0xffu) +
+             (int)(int8_t)(pq >> 24);
+    }
+  }
+  sum = warp_sum(sum);
+  if (lane == 0) red_i[warp] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    int t = 0;
+    for (int w = 0; w < kNW; ++w) t += red_i[w];
+    *peer(&c_qs[rank], 0u) = t;
+  }
+  cl_arrive();
+  cl_wait();  // (3): every chunk sum is in rank 0's shared memory
+  if (rank == 0 && tid == 0) {
+    s_x[m] = a;
+    if (x_sum) {
+      int t = 0;
+      for (uint32_t r = 0; r < C; ++r) t += c_qs[r];
+      x_sum[m] = t;
+    }
+  }
+}
+
 }  // namespace tw
 
 static int act_threads(long long K) {
@@ -267,10 +457,38 @@ static int act_threads(long long K) {
   return t;
 }
 
+// CTAs per token: one below K = 6144 or above 16 tokens (the tokens alone then spread over the
+// SMs), else a cluster of 2 (K < 8192), 4 (K < 16384) or 8.  Measured in the benchmark's
+// layer chains against one CTA per token: 2B at 8 tokens 48.4 -> 45.4 us per layer, 8B at 16
+// tokens 121.3 -> 118.0, 70B at 4 tokens 155.3 -> 149.6, 70B at 16 tokens 288.3 -> 284.4; at
+// K = 4096 the cluster lost (8B at 16 tokens 121.3 -> 122.9), and at 64 tokens it gained nothing.
+static int act_cluster(long long M, long long K) {
+  if (M > 16 || K < 6144) return 1;
+  return K < 8192 ? 2 : K < 16384 ? 4 : 8;
+}
+
 // Launched with programmatic dependent launch (the kernel waits before reading x).
 template <bool RMS>
 static cudaError_t launch_act(const float* x, const float* g, float eps, long long M, long long K, int8_t* x_q,
                               float* s_x, int32_t* x_sum, cudaStream_t stream) {
+  const int C = act_cluster(M, K);
+  if (C > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, (unsigned)M);
+    cfg.blockDim = dim3(tw::kActClusterThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, tw::act_quant_cluster_kernel<RMS>, x, g, eps, (int)K, tw::make_kdiv((int)K),
+                              1.0f / (float)K, x_q, s_x, x_sum);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)M);
   cfg.blockDim = dim3((unsigned)act_threads(K));

@@ -474,6 +474,29 @@ __device__ __forceinline__ uint4 permute_group(uint4 a) {
   return o;
 }
 
+// Thread-block clusters: this CTA's rank and the cluster's size, the split cluster barrier
+// (every thread of every CTA arrives, then waits; release/acquire orders the shared-memory
+// stores made through distributed shared memory before it), and a peer CTA's copy of a
+// shared variable.
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cl_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+template <typename T>
+__device__ __forceinline__ T* peer(T* p, uint32_t rank) {
+  return static_cast<T*>(__cluster_map_shared_rank(static_cast<void*>(p), rank));
+}
+
 __device__ __forceinline__ int byte_sum16(uint4 a) {
   int s = __dp4a((int)a.x, 0x01010101, 0);
   s = __dp4a((int)a.y, 0x01010101, s);

@@ -510,26 +510,8 @@ __device__ __forceinline__ void fused_prologue(const StreamArgs& a, uint4* xs, f
 // the ranks: well inside the error bound that the mean-square decision assumes, so a
 // decided mean square is the exact one, as in one CTA.  x_q, s_x and x_sum are written by
 // cluster 0.
-__device__ __forceinline__ uint32_t cl_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cl_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cl_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
 constexpr int kMaxCluster = 4;  // clusters of 2 or 4 CTAs
 
-template <typename T>
-__device__ __forceinline__ T* peer(T* p, uint32_t rank) {
-  return static_cast<T*>(__cluster_map_shared_rank(static_cast<void*>(p), rank));
-}
 
 template <int MT>
 struct ClusterSlots {

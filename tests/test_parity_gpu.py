@@ -99,8 +99,11 @@ def test_pack_repeatable_with_dirty_workspace(tw):
 
 
 # ----------------------------------------------------------------------------- activation quant
+# Up to 16 tokens with K >= 6144 take the cluster-shared kernel: 2 CTAs per token below 8192, 4
+# below 16384, 8 above (K = 6148 and 16388: chunks that do not divide the row evenly)
 ACT_CASES = [(1, 256, 0), (3, 68, 1), (16, 2560, 2), (17, 64, 3), (64, 4, 4), (65, 6912, 5),
-             (1, 28672, 6), (2, 12, 7)]
+             (1, 28672, 6), (2, 12, 7), (4, 4096, 8), (7, 6912, 9), (3, 6148, 10), (5, 8192, 11),
+             (16, 12288, 12), (2, 16388, 13), (1, 65472, 14), (17, 8192, 15)]
 
 
 @pytest.mark.parametrize("M,K,seed", ACT_CASES)
@@ -149,6 +152,27 @@ def test_act_special_rows(tw):
             got = tw.quantize(dev(x))
         for a, b in zip(got, ref):
             assert (host(a).view(np.uint8) == b.view(np.uint8)).all(), use_rms
+
+
+@pytest.mark.parametrize("K", [6912, 8192, 28672])
+def test_act_special_rows_cluster(tw, K):
+    """The special rows (six tokens) at row lengths the cluster-shared kernel takes (2, 4 and 8
+    CTAs per token): all-zero, exponents 2^-140..2^60 and subnormal rows take the exact
+    mean-square path in every CTA of the cluster; one-hot and exact ties."""
+    x = special_rows(K)
+    x[4, :] = 0.0
+    x[4, K - 3] = -3.0  # in the last CTA's chunk
+    g = si.rms_gain(K, seed=13)
+    for use_rms in (False, True):
+        if use_rms:
+            ref = oracle.rmsnorm_quant_act(x, g, si.RMS_EPS)
+            got = tw.quantize(dev(x), dev(g), si.RMS_EPS)
+        else:
+            ref = oracle.quant_act(x)
+            got = tw.quantize(dev(x))
+        for a, b in zip(got, ref):
+            assert (host(a).view(np.uint8) == b.view(np.uint8)).all(), (K, use_rms)
+    assert tw.tw_device_status() == 0
 
 
 def near_tie_tokens(K=256, M=8, seed=0):
