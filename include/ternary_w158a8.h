@@ -158,7 +158,7 @@ TW_API tw_status tw_pack_ternary_noalloc(const float *W, int64_t N, int64_t K, u
  *   s_x    [M] fp32 output: max|x| per token (the dequantisation uses s_x / 127).
  *   x_sum  [M] int32 output (sum of x_q per token), or NULL.
  * Requires 1 <= M <= 2^20, 4 <= K <= TW_MAX_K, K % 4 == 0.
- * One CTA per token; up to 16 tokens with K >= 6144, each token is shared by a thread-block
+ * One CTA per token; for 2 to 16 tokens with K >= 6144, each token is shared by a thread-block
  * cluster of 2, 4 or 8 CTAs (K < 8192, < 16384, above) that exchange their chunks' partial
  * results through distributed shared memory (the same bits).  Launched with programmatic
  * dependent launch; x is read only after the previous kernel on `stream` has finished.

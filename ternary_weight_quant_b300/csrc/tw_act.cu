@@ -457,13 +457,15 @@ static int act_threads(long long K) {
   return t;
 }
 
-// CTAs per token: one below K = 6144 or above 16 tokens (the tokens alone then spread over the
-// SMs), else a cluster of 2 (K < 8192), 4 (K < 16384) or 8.  Measured in the benchmark's
-// layer chains against one CTA per token: 2B at 8 tokens 48.4 -> 45.4 us per layer, 8B at 16
-// tokens 121.3 -> 118.0, 70B at 4 tokens 155.3 -> 149.6, 70B at 16 tokens 288.3 -> 284.4; at
-// K = 4096 the cluster lost (8B at 16 tokens 121.3 -> 122.9), and at 64 tokens it gained nothing.
+// CTAs per token: one below K = 6144, for one token, or above 16 tokens (the tokens alone then
+// spread over the SMs), else a cluster of 2 (K < 8192), 4 (K < 16384) or 8.  Measured in the
+// benchmark's layer chains against one CTA per token: 2B at 8 tokens 48.4 -> 45.1 us per
+// layer, 8B at 16 tokens 121.3 -> 117.7, 70B at 4 tokens 155.3 -> 149.7, 70B at 16 tokens
+// 288.3 -> 282.7; at K = 4096 the cluster lost (8B at 16 tokens 121.3 -> 122.9), at 64 tokens
+// it gained nothing, and at one token (the 2B step with separate quantisation, behind the
+// one-token decode kernel) it lost 1.2 us per layer.
 static int act_cluster(long long M, long long K) {
-  if (M > 16 || K < 6144) return 1;
+  if (M < 2 || M > 16 || K < 6144) return 1;
   return K < 8192 ? 2 : K < 16384 ? 4 : 8;
 }
 
