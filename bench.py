@@ -640,10 +640,16 @@ def measure(tw, workload: str, steps: int, warmup: int, world: int, separate: bo
         algo_per_call = ops_per_step / prod_calls_per_step
         peak, pk = measured_tensor_peak()
         achieved, unit, bound, peak_kind = algo_per_call / avg_launch_s / 1e12, "TFLOP/s", "tensor", pk
+    # the product kernels the library's dispatch takes for this workload's shapes
     if fused:
-        kern = "tw::gemv_decode_kernel (one token, quantisation fused)"
+        kern = {"2B": "tw::gemv_decode_kernel (one token, quantisation fused)",
+                "8B": "tw::gemv_decode_kernel (q|k|v, o) / gemv_stream_kernel (gate|up, down; one token, "
+                      "quantisation fused)",
+                "70B": "tw::gemv_stream_kernel (one token, quantisation fused)"}.get(model, "tw::gemv_decode_kernel")
+    elif M <= 4:
+        kern = "tw::gemv_stream_kernel / mma::gemv_mma_kernel / gemv_dp4a_kernel (by shape)"
     elif M <= 16:
-        kern = "tw::gemv_stream_kernel / gemv_dp4a_kernel"
+        kern = "tw::mma::gemv_mma_kernel (mma.sync) / gemm kernels (by shape)"
     else:
         kern = "tw::gemm::gemm_tok_kernel / gemm_tma_kernel (tcgen05)"
 
